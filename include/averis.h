@@ -1,0 +1,230 @@
+/*
+ * averis.h -- C ABI of libaveris.so: the Averis mean-residual split NVFP4
+ * linear layer (forward and backward) on NVIDIA B300 (sm_103a).
+ *
+ * The method: "The Curse and Blessing of Mean Bias in FP4-Quantized LLM
+ * Training" (arXiv 2603.10444).  Citations below use these keys:
+ *
+ *  [P1-method]   paper.rainbus.top summary "均值偏置的诅咒与祝福：FP4量化大语言模型训练",
+ *                section 方法步骤详情 (method details): mu_X = (1/l) 1^T X,
+ *                X_R = X - 1 mu_X, independent quantization of mu, X_R, W,
+ *                Y = 1 (mu_X W) + X_R W; the same for the output gradient D:
+ *                dX = 1 (mu_D W^T) + D_R W^T, dW = X_R^T D_R + l mu_X^T mu_D.
+ *  [P1-quant]    same page, background 块量化 (blockwise quantization) and
+ *                FP4量化 (NVFP4 uses E2M1 elements).
+ *  [P1-hadamard] same page, background Hadamard变换: 16x16 Hadamard on
+ *                [l, m/16, 16].
+ *  [P2-method]   paperlayer.ai summary "The Curse and Blessing of Mean Bias in
+ *                FP4-Quantized LLM Training", section 3 Method: the mean is
+ *                broadcast over tokens, never materialised.
+ *
+ * NVFP4 reading (the pages fix only "E2M1, one shared scale per block"):
+ * 16-element blocks along the GEMM's contraction axis, one E4M3 block scale,
+ * one binary32 tensor scale s_g = fl32(amax / 2688); every rounding is
+ * round-to-nearest-even with saturation.  Dequantized value =
+ * e2m1(code) * e4m3(scale) * s_g.
+ *
+ * Conventions for every call:
+ *  - Pointers marked "device" are device memory of the current CUDA device,
+ *    allocated and owned by the caller; the library allocates nothing and
+ *    keeps no state besides per-device kernel attributes.
+ *  - All work is enqueued on `stream`; a call returns as soon as it is
+ *    enqueued.  The status reports argument errors (nothing is enqueued then)
+ *    and launch errors.  Device-side wait timeouts are reported through
+ *    averis_last_device_error().
+ *  - bf16 inputs are row-major and 16-byte aligned; every device pointer must
+ *    be 16-byte aligned (256-byte for workspaces).
+ *  - Calls that share a workspace or an output must not overlap in time.
+ *  - Sizes: cols of every NVFP4 tensor and the m, n of a linear layer must be
+ *    multiples of 16; the token count l may be any value >= 1 (a partial last
+ *    16-block along l is zero-padded).
+ */
+#ifndef AVERIS_H
+#define AVERIS_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  AVERIS_OK = 0,
+  AVERIS_ERR_INVALID_ARG = 1,        /* bad size, null or misaligned pointer */
+  AVERIS_ERR_UNSUPPORTED_ARCH = 2,   /* current device is not sm_10x */
+  AVERIS_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed */
+  AVERIS_ERR_WORKSPACE_TOO_SMALL = 4,
+  AVERIS_ERR_TIMEOUT = 5             /* a device-side wait gave up (see averis_last_device_error) */
+} averis_status;
+
+/* flags */
+#define AVERIS_MEAN_SPLIT 1u  /* subtract the column mean (Averis); clear = vanilla NVFP4 */
+#define AVERIS_HADAMARD16 2u  /* rotate 16-blocks along each contraction axis by H16/4 ([P1-hadamard]) */
+#define AVERIS_OUT_BF16   4u  /* write Y / dX (and averis_gemm's output) as bf16; default binary32 */
+
+/*
+ * An NVFP4 tensor of logical shape [rows, cols], blocked along cols
+ * ([P1-quant]).  All pointers are device pointers owned by the caller.
+ *  codes        rows * averis_nvfp4_ld(cols) bytes, row-major; byte j of a row
+ *               holds element 2j in its low nibble and 2j+1 in its high nibble
+ *               (E2M1 code: bit 3 sign, bits 2..0 magnitude index).
+ *  scales       averis_nvfp4_scale_bytes(rows, cols) bytes of E4M3 block
+ *               scales, tiled for the tensor cores: tile (rb, kc) covers rows
+ *               128*rb .. +127 and blocks 4*kc .. +3; it sits at byte
+ *               512*(rb*ceil(cols/64) + kc) and stores (row r, block k) at
+ *               16*(r%32) + 4*((r%128)/32) + (k%4).  Padding entries are 0.
+ *  tensor_scale one binary32 s_g.
+ */
+typedef struct {
+  uint8_t* codes;
+  uint8_t* scales;
+  float* tensor_scale;
+  int64_t rows;
+  int64_t cols;
+} averis_nvfp4;
+
+/* Bytes per row of an NVFP4 code buffer: round_up(cols, 64) / 2. */
+int64_t averis_nvfp4_ld(int64_t cols);
+/* rows * averis_nvfp4_ld(cols). */
+size_t averis_nvfp4_code_bytes(int64_t rows, int64_t cols);
+/* 512 * ceil(rows/128) * ceil(cols/64). */
+size_t averis_nvfp4_scale_bytes(int64_t rows, int64_t cols);
+
+/*
+ * Forward state: what the forward pass produces and the backward pass reads.
+ * All buffers device, caller-owned, sized for an l x m activation:
+ *  x_row  X_R blocked along m, shape [l, m]  (operand of Y; may be scratch after fwd)
+ *  x_col  X_R^T blocked along l, shape [m, l] (operand of dW, kept for bwd)
+ *  mu_q   mu_X quantized along m, shape [1, m] (unused in vanilla mode)
+ *  mu     [m] binary32 column mean (unused in vanilla mode)
+ *  mu_hat [m] dequantized mean, unrotated basis (the dW outer product's left vector)
+ */
+typedef struct {
+  averis_nvfp4 x_row;
+  averis_nvfp4 x_col;
+  averis_nvfp4 mu_q;
+  float* mu;
+  float* mu_hat;
+} averis_fwd_state;
+
+/* Scratch bytes needed by averis_quantize / averis_quantize_weight for a rows x cols input. */
+size_t averis_quantize_workspace_bytes(int64_t rows, int64_t cols, unsigned flags);
+
+/*
+ * averis_quantize -- the fused mean-split quantize pass ([P1-method] steps
+ * mu = (1/l) 1^T T, T_R = T - 1 mu, independent Q_b of mu and T_R).
+ *  x         device bf16 [rows, cols] row-major (rows = tokens l, cols = features).
+ *  flags     AVERIS_MEAN_SPLIT: subtract the column mean (else T_R = T, and mu,
+ *            mu_q, mu_hat are ignored and may be NULL); AVERIS_HADAMARD16.
+ *  mu        device [cols] binary32 column mean (output).
+ *  mu_q      NVFP4 [1, cols] of the mean (output; rotated basis under HADAMARD16).
+ *  mu_hat    device [cols] dequantized mean in the unrotated basis (output).
+ *  out_row   NVFP4 [rows, cols] of T_R blocked along cols (output, NULL to skip).
+ *  out_col   NVFP4 [cols, rows] of T_R^T blocked along rows (output, NULL to skip).
+ *  workspace device scratch of averis_quantize_workspace_bytes() bytes.
+ * Errors: INVALID_ARG (cols % 16, shapes of the outputs, alignment),
+ * WORKSPACE_TOO_SMALL, UNSUPPORTED_ARCH, CUDA.
+ */
+averis_status averis_quantize(const void* x, int64_t rows, int64_t cols, unsigned flags,
+                              float* mu, const averis_nvfp4* mu_q, float* mu_hat,
+                              const averis_nvfp4* out_row, const averis_nvfp4* out_col,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * averis_quantize_weight -- W_bar = Q_b(W) ([P1-method]); no mean split.
+ *  w       device bf16 [m, n] row-major (Y = X W).
+ *  w_n     NVFP4 [m, n] blocked along n: the B operand of dX = D W^T (output).
+ *  w_m     NVFP4 [n, m] blocked along m: the B operand of Y = X W (output).
+ *  flags   AVERIS_HADAMARD16 rotates along the blocking axis; MEAN_SPLIT is ignored.
+ */
+averis_status averis_quantize_weight(const void* w, int64_t m, int64_t n, unsigned flags,
+                                     const averis_nvfp4* w_n, const averis_nvfp4* w_m,
+                                     void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * averis_rank1 -- the rank-one row r = deq(mu_q) deq(w)^T ([P1-method]: the
+ * mu_bar W_bar and mu_bar W_bar^T terms), binary32.
+ *  mu_q  NVFP4 [1, K];  w  NVFP4 [N, K] blocked along K;  out  device [N].
+ */
+averis_status averis_rank1(const averis_nvfp4* mu_q, const averis_nvfp4* w, float* out,
+                           cudaStream_t stream);
+
+/*
+ * averis_gemm -- block-scaled NVFP4 GEMM on the tcgen05 tensor cores with the
+ * Averis epilogue:
+ *   out[i][j] = s_a s_b sum_k a[i][k] b[j][k] + col_add[j] + outer_scale * row_vec[i] * col_vec[j]
+ *  a        NVFP4 [M, K];  b  NVFP4 [N, K] (both blocked along K).
+ *  col_add  device [N] or NULL (the broadcast mean term of Y and dX).
+ *  row_vec, col_vec  device [M], [N] or both NULL (the l mu_X^T mu_D term of dW).
+ *  out      device [M, ldo] binary32, or bf16 with AVERIS_OUT_BF16; ldo >= N,
+ *           ldo * element size a multiple of 16 bytes.
+ */
+averis_status averis_gemm(const averis_nvfp4* a, const averis_nvfp4* b,
+                          const float* col_add, const float* row_vec, const float* col_vec,
+                          float outer_scale, void* out, int64_t ldo, unsigned flags,
+                          cudaStream_t stream);
+
+/* Scratch bytes of averis_linear_fwd / averis_linear_bwd (and the nvfp4_ ones). */
+size_t averis_linear_fwd_workspace_bytes(int64_t l, int64_t m, int64_t n, unsigned flags);
+size_t averis_linear_bwd_workspace_bytes(int64_t l, int64_t m, int64_t n, unsigned flags);
+
+/*
+ * averis_linear_fwd -- Y = 1 (mu_bar_X W_bar) + X_bar_R W_bar ([P1-method]
+ * forward equation; the mean term is added in the GEMM epilogue, never
+ * materialised, [P2-method]).
+ *  x      device bf16 [l, m];  w_m  NVFP4 [n, m] from averis_quantize_weight.
+ *  y      device [l, n] binary32 (bf16 with AVERIS_OUT_BF16).
+ *  state  forward state (outputs), see averis_fwd_state.
+ *  flags  AVERIS_MEAN_SPLIT must be set (see nvfp4_linear_fwd for vanilla).
+ */
+averis_status averis_linear_fwd(const void* x, int64_t l, int64_t m, int64_t n,
+                                const averis_nvfp4* w_m, unsigned flags, void* y,
+                                const averis_fwd_state* state,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * averis_linear_bwd -- dX = 1 (mu_bar_D W_bar^T) + D_bar_R W_bar^T and
+ * dW = X_bar_R^T D_bar_R + l mu_bar_X^T mu_bar_D ([P1-method] gradient
+ * equations; cross terms dropped as written there).
+ *  d      device bf16 [l, n];  w_n  NVFP4 [m, n] from averis_quantize_weight.
+ *  state  the forward state of the same layer.
+ *  dx     device [l, m] binary32 (bf16 with AVERIS_OUT_BF16);  dw  device [m, n] binary32.
+ */
+averis_status averis_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n,
+                                const averis_fwd_state* state, const averis_nvfp4* w_n,
+                                unsigned flags, void* dx, float* dw,
+                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Vanilla NVFP4 linear layer, the comparison path: Y = Q(X) Q(W),
+ * dX = Q(D) Q(W)^T, dW = Q(X)^T Q(D).  Same arguments as the Averis calls;
+ * AVERIS_MEAN_SPLIT is ignored, state.mu / mu_q / mu_hat are unused.
+ */
+averis_status nvfp4_linear_fwd(const void* x, int64_t l, int64_t m, int64_t n,
+                               const averis_nvfp4* w_m, unsigned flags, void* y,
+                               const averis_fwd_state* state,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+averis_status nvfp4_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n,
+                               const averis_fwd_state* state, const averis_nvfp4* w_n,
+                               unsigned flags, void* dx, float* dw,
+                               void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* Human-readable name of a status. */
+const char* averis_status_string(averis_status status);
+
+/*
+ * Reads and clears the device error word that kernels set when a bounded
+ * wait gives up.  Synchronizes `stream`.  Returns AVERIS_OK or AVERIS_ERR_TIMEOUT;
+ * *where (if not NULL) receives the code of the wait that gave up.
+ */
+averis_status averis_last_device_error(cudaStream_t stream, int* where);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int averis_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* AVERIS_H */

@@ -1,0 +1,491 @@
+// C ABI of libaveris.so: argument checks, workspace carving, tensor-map
+// encoding and kernel launches.  Declarations and per-call contracts are in
+// include/averis.h.
+#include <cstdint>
+#include <cstring>
+#include <algorithm>
+#include <mutex>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "averis.h"
+#include "gemm.cuh"
+#include "quant.cuh"
+
+namespace {
+
+using namespace averis;
+
+constexpr int kMaxDevices = 64;
+constexpr int kStatsTargetCtas = 1184;  // row-block count target of the stats pass
+
+__device__ int g_device_error = 0;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int cc_major = 0, cc_minor = 0;
+  int* err_word = nullptr;
+  bool attrs_set = false;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_mutex;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+averis_status set_attrs();
+
+// Per-device setup: SM count, architecture check, error-word address, kernel attributes.
+averis_status device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AVERIS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return AVERIS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceInfo& d = g_dev[dev];
+  if (!d.ready) {
+    if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return AVERIS_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+      return AVERIS_ERR_CUDA;
+    if (cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return AVERIS_ERR_CUDA;
+    if (d.cc_major != 10 || d.cc_minor != 3) return AVERIS_ERR_UNSUPPORTED_ARCH;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return AVERIS_ERR_CUDA;
+    d.err_word = static_cast<int*>(addr);
+    if (g_encode == nullptr) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+              cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return AVERIS_ERR_CUDA;
+      g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    d.ready = true;
+  }
+  if (!d.attrs_set) {
+    averis_status st = set_attrs();
+    if (st != AVERIS_OK) return st;
+    d.attrs_set = true;
+  }
+  *out = &d;
+  return AVERIS_OK;
+}
+
+averis_status set_attrs() {
+  if (cudaFuncSetAttribute(split_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+      cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(split_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+      cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GemmCfg<128>::SMEM) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GemmCfg<128>::SMEM) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  return AVERIS_OK;
+}
+
+averis_status launch_status() { return cudaGetLastError() == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA; }
+
+// ------------------------------------------------------------ geometry --
+
+struct StatsGeom {
+  int strips, nrb;
+  int64_t rows_per;
+};
+
+StatsGeom stats_geom(int64_t R, int64_t C) {
+  StatsGeom g;
+  g.strips = (int)cdiv(C, 256);
+  int64_t nrb = cdiv(kStatsTargetCtas, g.strips);
+  nrb = std::max<int64_t>(1, std::min<int64_t>(nrb, cdiv(R, 64)));
+  int64_t rp = cdiv(R, nrb);
+  rp = cdiv(rp, 32) * 32;
+  g.rows_per = rp;
+  g.nrb = (int)cdiv(R, rp);
+  return g;
+}
+
+size_t quant_ws_bytes(int64_t R, int64_t C) {
+  const StatsGeom g = stats_geom(R, C);
+  return align256(kCtrlWords * sizeof(unsigned)) + align256((size_t)g.nrb * (size_t)C * sizeof(ColPartial));
+}
+
+bool nvfp4_ok(const averis_nvfp4* t, int64_t rows, int64_t cols) {
+  return t != nullptr && t->codes != nullptr && t->scales != nullptr && t->tensor_scale != nullptr &&
+         t->rows == rows && t->cols == cols && aligned(t->codes, 16) && aligned(t->scales, 16) &&
+         aligned(t->tensor_scale, 4);
+}
+
+// ------------------------------------------------------------- quantize --
+
+averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags, float* mu, const averis_nvfp4* mu_q,
+                            float* mu_hat, const averis_nvfp4* out_row, const averis_nvfp4* out_col, void* ws,
+                            size_t ws_bytes, cudaStream_t s) {
+  if (x == nullptr || R < 1 || C < 16 || C % 16 != 0 || !aligned(x, 16)) return AVERIS_ERR_INVALID_ARG;
+  if (R > (int64_t)1 << 31 || C > (int64_t)1 << 31) return AVERIS_ERR_INVALID_ARG;
+  const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
+  const bool had = (flags & AVERIS_HADAMARD16) != 0;
+  if (out_row != nullptr && !nvfp4_ok(out_row, R, C)) return AVERIS_ERR_INVALID_ARG;
+  if (out_col != nullptr && !nvfp4_ok(out_col, C, R)) return AVERIS_ERR_INVALID_ARG;
+  if (split && (mu == nullptr || mu_hat == nullptr || !aligned(mu, 16) || !aligned(mu_hat, 16) ||
+                !nvfp4_ok(mu_q, 1, C)))
+    return AVERIS_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256)) return AVERIS_ERR_INVALID_ARG;
+  if (ws_bytes < quant_ws_bytes(R, C)) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* dev = nullptr;
+  averis_status st = device_info(&dev);
+  if (st != AVERIS_OK) return st;
+
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  unsigned* ctrl = reinterpret_cast<unsigned*>(w);
+  ColPartial* part = reinterpret_cast<ColPartial*>(w + align256(kCtrlWords * sizeof(unsigned)));
+  const StatsGeom g = stats_geom(R, C);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+
+  colstats_partial_kernel<<<dim3(g.strips, g.nrb), 256, 0, s>>>(xb, R, C, g.rows_per, part, ctrl);
+  if ((st = launch_status()) != AVERIS_OK) return st;
+
+  FinalizeParams fp{};
+  fp.part = part;
+  fp.nrb = g.nrb;
+  fp.R = R;
+  fp.C = C;
+  fp.split = split ? 1 : 0;
+  fp.hadamard = had ? 1 : 0;
+  fp.mu = mu;
+  fp.ctrl = ctrl;
+  if (split) {
+    fp.mu_codes = mu_q->codes;
+    fp.mu_scales = mu_q->scales;
+    fp.mu_ts = mu_q->tensor_scale;
+    fp.mu_hat = mu_hat;
+  }
+  fp.kc = cdiv(C, 64);
+  colstats_finalize_kernel<<<(unsigned)cdiv(C, 256), 256, 0, s>>>(fp);
+  if ((st = launch_status()) != AVERIS_OK) return st;
+
+  if (out_row == nullptr && out_col == nullptr) return AVERIS_OK;
+  QuantParams qp{};
+  qp.x = xb;
+  qp.R = R;
+  qp.C = C;
+  qp.mu = split ? mu : nullptr;
+  qp.ctrl = ctrl;
+  qp.hadamard = had ? 1 : 0;
+  if (out_row != nullptr) {
+    qp.row_codes = out_row->codes;
+    qp.row_scales = out_row->scales;
+    qp.row_ts = out_row->tensor_scale;
+    qp.row_ld = averis_nvfp4_ld(C);
+    qp.row_kc = cdiv(C, 64);
+  }
+  if (out_col != nullptr) {
+    qp.col_codes = out_col->codes;
+    qp.col_scales = out_col->scales;
+    qp.col_ts = out_col->tensor_scale;
+    qp.col_ld = averis_nvfp4_ld(R);
+    qp.col_kc = cdiv(R, 64);
+  }
+  qp.tiles_r = (int)cdiv(R, kQTile);
+  qp.tiles_c = (int)cdiv(C, kQTile);
+  const int ntiles = qp.tiles_r * qp.tiles_c;
+  const int grid = (int)std::min<int64_t>(ntiles, 2 * (int64_t)dev->sms);
+  if (had) {
+    split_quant_kernel<true><<<grid, kQThreads, kQSmem, s>>>(qp);
+    if ((st = launch_status()) != AVERIS_OK) return st;
+  }
+  split_quant_kernel<false><<<grid, kQThreads, kQSmem, s>>>(qp);
+  return launch_status();
+}
+
+// ----------------------------------------------------------------- GEMM --
+
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const float* col_add, const float* row_vec,
+                        const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s) {
+  if (a == nullptr || b == nullptr || out == nullptr) return AVERIS_ERR_INVALID_ARG;
+  const int64_t M = a->rows, N = b->rows, K = a->cols;
+  if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || b->cols != K) return AVERIS_ERR_INVALID_ARG;
+  if (M > (int64_t)1 << 30 || N > (int64_t)1 << 30 || K > (int64_t)1 << 30) return AVERIS_ERR_INVALID_ARG;
+  if (!nvfp4_ok(a, M, K) || !nvfp4_ok(b, N, K)) return AVERIS_ERR_INVALID_ARG;
+  const bool bf16 = (flags & AVERIS_OUT_BF16) != 0;
+  const int64_t esz = bf16 ? 2 : 4;
+  if (ldo < N || (ldo * esz) % 16 != 0 || !aligned(out, 16)) return AVERIS_ERR_INVALID_ARG;
+  if ((row_vec == nullptr) != (col_vec == nullptr)) return AVERIS_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  averis_status st = device_info(&dev);
+  if (st != AVERIS_OK) return st;
+
+  constexpr int BN = 128;
+  using Cfg = GemmCfg<BN>;
+  const int64_t ld = averis_nvfp4_ld(K);
+  CUtensorMap ta, tb, td;
+  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->codes, (uint64_t)ld, (uint64_t)M, (uint64_t)ld, Cfg::BKB,
+                 Cfg::BM))
+    return AVERIS_ERR_CUDA;
+  if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b->codes, (uint64_t)ld, (uint64_t)N, (uint64_t)ld, Cfg::BKB,
+                 BN))
+    return AVERIS_ERR_CUDA;
+  if (!encode_2d(&td, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, (uint64_t)N,
+                 (uint64_t)M, (uint64_t)(ldo * esz), bf16 ? 64u : 32u, 32u))
+    return AVERIS_ERR_CUDA;
+
+  GemmParams p{};
+  p.M = (int)M;
+  p.N = (int)N;
+  p.K = (int)K;
+  p.kc = (int)cdiv(K, 64);
+  p.rb_b = (int)cdiv(N, 128);
+  p.sfa = a->scales;
+  p.sfb = b->scales;
+  p.ts_a = a->tensor_scale;
+  p.ts_b = b->tensor_scale;
+  p.col_add = col_add;
+  p.row_vec = row_vec;
+  p.col_vec = col_vec;
+  p.outer = outer;
+  p.err = dev->err_word;
+  const int64_t ntiles = cdiv(M, Cfg::BM) * cdiv(N, BN);
+  const int grid = (int)std::min<int64_t>(ntiles, dev->sms);
+  if (bf16)
+    gemm_nvfp4_kernel<BN, true><<<grid, 192, Cfg::SMEM, s>>>(ta, tb, td, p);
+  else
+    gemm_nvfp4_kernel<BN, false><<<grid, 192, Cfg::SMEM, s>>>(ta, tb, td, p);
+  return launch_status();
+}
+
+averis_status rank1_impl(const averis_nvfp4* mu_q, const averis_nvfp4* w, float* out, cudaStream_t s) {
+  if (w == nullptr || mu_q == nullptr || out == nullptr || !aligned(out, 4)) return AVERIS_ERR_INVALID_ARG;
+  const int64_t N = w->rows, K = w->cols;
+  if (N < 1 || K < 16 || K % 16 != 0) return AVERIS_ERR_INVALID_ARG;
+  if (!nvfp4_ok(w, N, K) || !nvfp4_ok(mu_q, 1, K)) return AVERIS_ERR_INVALID_ARG;
+  DeviceInfo* dev = nullptr;
+  averis_status st = device_info(&dev);
+  if (st != AVERIS_OK) return st;
+  rank1_gemv_kernel<<<(unsigned)cdiv(N, 8), 256, 0, s>>>(mu_q->codes, mu_q->scales, mu_q->tensor_scale, w->codes,
+                                                         w->scales, w->tensor_scale, averis_nvfp4_ld(K), N, K,
+                                                         cdiv(K, 64), out);
+  return launch_status();
+}
+
+// --------------------------------------------------------------- layers --
+
+struct Carver {
+  uint8_t* p;
+  size_t used = 0;
+  explicit Carver(void* base) : p(static_cast<uint8_t*>(base)) {}
+  void* take(size_t bytes) {
+    void* r = p + used;
+    used += align256(bytes);
+    return r;
+  }
+};
+
+size_t nvfp4_bytes(int64_t rows, int64_t cols) {
+  return align256(averis_nvfp4_code_bytes(rows, cols)) + align256(averis_nvfp4_scale_bytes(rows, cols)) + 256;
+}
+
+averis_nvfp4 carve_nvfp4(Carver& c, int64_t rows, int64_t cols) {
+  averis_nvfp4 t;
+  t.codes = static_cast<uint8_t*>(c.take(averis_nvfp4_code_bytes(rows, cols)));
+  t.scales = static_cast<uint8_t*>(c.take(averis_nvfp4_scale_bytes(rows, cols)));
+  t.tensor_scale = static_cast<float*>(c.take(sizeof(float)));
+  t.rows = rows;
+  t.cols = cols;
+  return t;
+}
+
+size_t fwd_ws(int64_t l, int64_t m, int64_t n) { return quant_ws_bytes(l, m) + align256((size_t)n * 4); }
+
+size_t bwd_ws(int64_t l, int64_t m, int64_t n) {
+  return quant_ws_bytes(l, n) + nvfp4_bytes(l, n) + nvfp4_bytes(n, l) + nvfp4_bytes(1, n) +
+         2 * align256((size_t)n * 4) + align256((size_t)m * 4);
+}
+
+averis_status linear_fwd_impl(const void* x, int64_t l, int64_t m, int64_t n, const averis_nvfp4* w_m, unsigned flags,
+                              void* y, const averis_fwd_state* st, void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (st == nullptr || w_m == nullptr || y == nullptr) return AVERIS_ERR_INVALID_ARG;
+  if (l < 1 || m < 16 || n < 16 || m % 16 || n % 16) return AVERIS_ERR_INVALID_ARG;
+  if (!nvfp4_ok(w_m, n, m)) return AVERIS_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256)) return AVERIS_ERR_INVALID_ARG;
+  if (ws_bytes < fwd_ws(l, m, n)) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
+  const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
+  Carver c(ws);
+  void* qws = c.take(quant_ws_bytes(l, m));
+  float* r_x = static_cast<float*>(c.take((size_t)n * 4));
+  averis_status r = quantize_impl(x, l, m, flags, st->mu, &st->mu_q, st->mu_hat, &st->x_row, &st->x_col, qws,
+                                  quant_ws_bytes(l, m), s);
+  if (r != AVERIS_OK) return r;
+  if (split) {
+    if ((r = rank1_impl(&st->mu_q, w_m, r_x, s)) != AVERIS_OK) return r;
+  }
+  return gemm_impl(&st->x_row, w_m, split ? r_x : nullptr, nullptr, nullptr, 0.f, y, n, flags, s);
+}
+
+averis_status linear_bwd_impl(const void* d, int64_t l, int64_t m, int64_t n, const averis_fwd_state* st,
+                              const averis_nvfp4* w_n, unsigned flags, void* dx, float* dw, void* ws,
+                              size_t ws_bytes, cudaStream_t s) {
+  if (st == nullptr || w_n == nullptr || dx == nullptr || dw == nullptr) return AVERIS_ERR_INVALID_ARG;
+  if (l < 1 || m < 16 || n < 16 || m % 16 || n % 16) return AVERIS_ERR_INVALID_ARG;
+  if (!nvfp4_ok(w_n, m, n) || !nvfp4_ok(&st->x_col, m, l)) return AVERIS_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256)) return AVERIS_ERR_INVALID_ARG;
+  if (ws_bytes < bwd_ws(l, m, n)) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
+  const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
+  if (split && (st->mu_hat == nullptr)) return AVERIS_ERR_INVALID_ARG;
+  Carver c(ws);
+  void* qws = c.take(quant_ws_bytes(l, n));
+  averis_nvfp4 d_row = carve_nvfp4(c, l, n);
+  averis_nvfp4 d_col = carve_nvfp4(c, n, l);
+  averis_nvfp4 mu_q = carve_nvfp4(c, 1, n);
+  float* mu = static_cast<float*>(c.take((size_t)n * 4));
+  float* mu_hat = static_cast<float*>(c.take((size_t)n * 4));
+  float* r_d = static_cast<float*>(c.take((size_t)m * 4));
+  averis_status r = quantize_impl(d, l, n, flags, mu, &mu_q, mu_hat, &d_row, &d_col, qws, quant_ws_bytes(l, n), s);
+  if (r != AVERIS_OK) return r;
+  if (split) {
+    if ((r = rank1_impl(&mu_q, w_n, r_d, s)) != AVERIS_OK) return r;
+  }
+  if ((r = gemm_impl(&d_row, w_n, split ? r_d : nullptr, nullptr, nullptr, 0.f, dx, m, flags, s)) != AVERIS_OK)
+    return r;
+  return gemm_impl(&st->x_col, &d_col, nullptr, split ? st->mu_hat : nullptr, split ? mu_hat : nullptr, (float)l, dw,
+                   n, flags & ~AVERIS_OUT_BF16, s);
+}
+
+}  // namespace
+
+// ================================================================ C ABI ==
+
+extern "C" {
+
+int64_t averis_nvfp4_ld(int64_t cols) { return cdiv(cols, 64) * 32; }
+
+size_t averis_nvfp4_code_bytes(int64_t rows, int64_t cols) {
+  return (size_t)rows * (size_t)averis_nvfp4_ld(cols);
+}
+
+size_t averis_nvfp4_scale_bytes(int64_t rows, int64_t cols) {
+  return (size_t)512 * (size_t)cdiv(rows, 128) * (size_t)cdiv(cols, 64);
+}
+
+size_t averis_quantize_workspace_bytes(int64_t rows, int64_t cols, unsigned flags) {
+  (void)flags;
+  if (rows < 1 || cols < 1) return 0;
+  return quant_ws_bytes(rows, cols);
+}
+
+averis_status averis_quantize(const void* x, int64_t rows, int64_t cols, unsigned flags, float* mu,
+                              const averis_nvfp4* mu_q, float* mu_hat, const averis_nvfp4* out_row,
+                              const averis_nvfp4* out_col, void* workspace, size_t workspace_bytes,
+                              cudaStream_t stream) {
+  return quantize_impl(x, rows, cols, flags, mu, mu_q, mu_hat, out_row, out_col, workspace, workspace_bytes, stream);
+}
+
+averis_status averis_quantize_weight(const void* w, int64_t m, int64_t n, unsigned flags, const averis_nvfp4* w_n,
+                                     const averis_nvfp4* w_m, void* workspace, size_t workspace_bytes,
+                                     cudaStream_t stream) {
+  if (w_n == nullptr && w_m == nullptr) return AVERIS_ERR_INVALID_ARG;
+  return quantize_impl(w, m, n, flags & AVERIS_HADAMARD16, nullptr, nullptr, nullptr, w_n, w_m, workspace,
+                       workspace_bytes, stream);
+}
+
+averis_status averis_rank1(const averis_nvfp4* mu_q, const averis_nvfp4* w, float* out, cudaStream_t stream) {
+  return rank1_impl(mu_q, w, out, stream);
+}
+
+averis_status averis_gemm(const averis_nvfp4* a, const averis_nvfp4* b, const float* col_add, const float* row_vec,
+                          const float* col_vec, float outer_scale, void* out, int64_t ldo, unsigned flags,
+                          cudaStream_t stream) {
+  return gemm_impl(a, b, col_add, row_vec, col_vec, outer_scale, out, ldo, flags, stream);
+}
+
+size_t averis_linear_fwd_workspace_bytes(int64_t l, int64_t m, int64_t n, unsigned flags) {
+  (void)flags;
+  if (l < 1 || m < 1 || n < 1) return 0;
+  return fwd_ws(l, m, n);
+}
+
+size_t averis_linear_bwd_workspace_bytes(int64_t l, int64_t m, int64_t n, unsigned flags) {
+  (void)flags;
+  if (l < 1 || m < 1 || n < 1) return 0;
+  return bwd_ws(l, m, n);
+}
+
+averis_status averis_linear_fwd(const void* x, int64_t l, int64_t m, int64_t n, const averis_nvfp4* w_m,
+                                unsigned flags, void* y, const averis_fwd_state* state, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  if (!(flags & AVERIS_MEAN_SPLIT)) return AVERIS_ERR_INVALID_ARG;
+  return linear_fwd_impl(x, l, m, n, w_m, flags, y, state, workspace, workspace_bytes, stream);
+}
+
+averis_status averis_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n, const averis_fwd_state* state,
+                                const averis_nvfp4* w_n, unsigned flags, void* dx, float* dw, void* workspace,
+                                size_t workspace_bytes, cudaStream_t stream) {
+  if (!(flags & AVERIS_MEAN_SPLIT)) return AVERIS_ERR_INVALID_ARG;
+  return linear_bwd_impl(d, l, m, n, state, w_n, flags, dx, dw, workspace, workspace_bytes, stream);
+}
+
+averis_status nvfp4_linear_fwd(const void* x, int64_t l, int64_t m, int64_t n, const averis_nvfp4* w_m,
+                               unsigned flags, void* y, const averis_fwd_state* state, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  return linear_fwd_impl(x, l, m, n, w_m, flags & ~AVERIS_MEAN_SPLIT, y, state, workspace, workspace_bytes, stream);
+}
+
+averis_status nvfp4_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n, const averis_fwd_state* state,
+                               const averis_nvfp4* w_n, unsigned flags, void* dx, float* dw, void* workspace,
+                               size_t workspace_bytes, cudaStream_t stream) {
+  return linear_bwd_impl(d, l, m, n, state, w_n, flags & ~AVERIS_MEAN_SPLIT, dx, dw, workspace, workspace_bytes,
+                         stream);
+}
+
+const char* averis_status_string(averis_status status) {
+  switch (status) {
+    case AVERIS_OK: return "ok";
+    case AVERIS_ERR_INVALID_ARG: return "invalid argument";
+    case AVERIS_ERR_UNSUPPORTED_ARCH: return "unsupported architecture (needs sm_103)";
+    case AVERIS_ERR_CUDA: return "CUDA error";
+    case AVERIS_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case AVERIS_ERR_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+averis_status averis_last_device_error(cudaStream_t stream, int* where) {
+  DeviceInfo* dev = nullptr;
+  averis_status st = device_info(&dev);
+  if (st != AVERIS_OK) return st;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return AVERIS_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return AVERIS_ERR_CUDA;
+  if (v != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return AVERIS_ERR_CUDA;
+  }
+  if (where != nullptr) *where = v;
+  return v == 0 ? AVERIS_OK : AVERIS_ERR_TIMEOUT;
+}
+
+int averis_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,315 @@
+// Block-scaled NVFP4 GEMM on the 5th-generation tensor cores (tcgen05) with
+// the Averis epilogue.
+//
+//   out[i][j] = s_a s_b * sum_k A[i][k] B[j][k] + col_add[j] + outer * u[i] v[j]
+//
+// A [M, K] and B [N, K] are NVFP4 (E2M1 codes, E4M3 scale per 16 along K);
+// the broadcast term col_add is the 1 (mu_bar W_bar) / 1 (mu_bar_D W_bar^T)
+// row of the forward and input-gradient equations, and outer * u v^T is the
+// l mu_bar_X^T mu_bar_D term of the weight gradient (paper.rainbus.top
+// summary "均值偏置的诅咒与祝福：FP4量化大语言模型训练", section 方法步骤详情;
+// the mean term is broadcast, never materialised: paperlayer.ai summary,
+// section 3 Method).
+//
+// Design: persistent CTAs (one per SM), 128 x BN output tiles, K tiles of 256
+// elements (128 bytes of codes per row).  Warp roles:
+//   warp 0     TMA producer: codes by 2-D tensor TMA (128-byte swizzle),
+//              block scales by 1-D bulk copies, into a STAGES-deep ring.
+//   warp 1     TMEM owner and MMA issuer: scale chunks SMEM->TMEM with
+//              tcgen05.cp, then tcgen05.mma kind::mxf4nvf4 (K = 64 per
+//              instruction) accumulating in TMEM; tcgen05.commit frees the
+//              SMEM stage and, after the last K tile, hands the accumulator
+//              to the epilogue.
+//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, alpha scaling and
+//              the rank-one terms in binary32, SMEM staging (128-byte
+//              swizzle) and TMA tensor stores (which clip ragged edges).
+// Two accumulator buffers (BN = 128) let the epilogue of tile t overlap the
+// main loop of tile t+1.  Every wait is bounded; on timeout the kernel sets
+// the error word, drains its own tensor-core work and frees its TMEM.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "ptx.cuh"
+
+namespace averis {
+
+struct GemmParams {
+  int M, N, K;
+  int kc;        // ceil(K / 64): 64-element scale chunks per row chunk (same for A and B)
+  int rb_b;      // ceil(N / 128): row chunks of B's scales
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  const float* ts_a;
+  const float* ts_b;
+  const float* col_add;  // [N] or null
+  const float* row_vec;  // [M] or null
+  const float* col_vec;  // [N] or null
+  float outer;
+  int* err;
+};
+
+enum : int { kErrNone = 0, kErrProducer = 1, kErrMma = 2, kErrEpilogue = 3, kErrDrain = 4 };
+
+constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clock
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int BM = 128;
+  static constexpr int BKB = 128;  // bytes of codes per row per K tile (256 elements)
+  static constexpr int STAGES = BN == 128 ? 4 : 3;
+  static constexpr int ACC_BUFS = BN == 128 ? 2 : 1;
+  static constexpr int A_BYTES = BM * BKB;
+  static constexpr int B_BYTES = BN * BKB;
+  static constexpr int SFA_BYTES = 4 * 512;
+  static constexpr int SFB_BYTES = (BN / 128) * 4 * 512;
+  static constexpr int EPI_BUF = 32 * 128;        // one warp's 32 rows x 128 bytes
+  static constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;
+  static constexpr int OFF_A = 0;
+  static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
+  static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
+  static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
+  static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
+  static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+  static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
+  // TMEM columns: accumulators, then per stage 16 SFA columns + BN/8 SFB columns
+  static constexpr int SF_BASE = ACC_BUFS * BN;
+  static constexpr int SFB_COLS_PER_STEP = BN / 32;
+  static constexpr int SF_STAGE_COLS = 16 + 4 * SFB_COLS_PER_STEP;
+  static constexpr int TMEM_COLS = 512;
+  static_assert(OFF_EPI % 1024 == 0, "epilogue staging must be 1024-byte aligned");
+  static_assert(SF_BASE + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM overflow");
+  // instruction descriptor: E2M1 x E2M1 (format 1), K-major A and B, UE4M3 scales,
+  // N >> 3 at bit 17, M >> 4 at bit 24
+  static constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+};
+
+template <int BN, bool BF16_OUT>
+__global__ void __launch_bounds__(192, 1)
+    gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int STAGES = Cfg::STAGES;
+  extern __shared__ uint8_t gsm_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&tfull[a], 1);
+      ptx::mbar_init(&tempty[a], 4);
+    }
+    ptx::mbar_init(drain, 1);
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmB);
+    ptx::prefetch_tmap(&tmD);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_slot, Cfg::TMEM_COLS);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int num_m = (p.M + Cfg::BM - 1) / Cfg::BM;
+  const int num_n = (p.N + BN - 1) / BN;
+  const int ntiles = num_m * num_n;
+  const int nkt = (p.kc + 3) / 4;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int mt = tile % num_m, nt = tile / num_m;
+        for (int kt = 0; kt < nkt; ++kt) {
+          if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, kWaitLimit)) {
+            atomicExch(p.err, kErrProducer);
+            goto done;
+          }
+          const int ns = min(4, p.kc - 4 * kt);
+          int nsfb = 0;
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) nsfb += (nt * (BN / 128) + h) < p.rb_b ? 1 : 0;
+          const uint32_t bytes = Cfg::A_BYTES + Cfg::B_BYTES + (uint32_t)ns * 512u * (1u + (uint32_t)nsfb);
+          ptx::mbar_arrive_expect_tx(&full[stage], bytes);
+          ptx::tma_load_2d(smem + Cfg::OFF_A + stage * Cfg::A_BYTES, &tmA, kt * Cfg::BKB, mt * Cfg::BM, &full[stage]);
+          ptx::tma_load_2d(smem + Cfg::OFF_B + stage * Cfg::B_BYTES, &tmB, kt * Cfg::BKB, nt * BN, &full[stage]);
+          ptx::bulk_load(smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES, p.sfa + ((int64_t)mt * p.kc + 4 * kt) * 512,
+                         ns * 512u, &full[stage]);
+#pragma unroll
+          for (int h = 0; h < BN / 128; ++h) {
+            const int rb = nt * (BN / 128) + h;
+            if (rb < p.rb_b)
+              ptx::bulk_load(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES + h * 2048,
+                             p.sfb + ((int64_t)rb * p.kc + 4 * kt) * 512, ns * 512u, &full[stage]);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool issued = false;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        const int acc = Cfg::ACC_BUFS == 2 ? (it & 1) : 0;
+        const uint32_t acc_phase = Cfg::ACC_BUFS == 2 ? ((it >> 1) & 1) : (it & 1);
+        if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitLimit)) {
+          atomicExch(p.err, kErrMma);
+          break;
+        }
+        ptx::tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+        bool ok = true;
+        for (int kt = 0; kt < nkt; ++kt) {
+          if (!ptx::mbar_wait(&full[stage], phase, kWaitLimit)) {
+            atomicExch(p.err, kErrMma);
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const int ns = min(4, p.kc - 4 * kt);
+          const uint32_t sfa_t = tmem + (uint32_t)(Cfg::SF_BASE + stage * Cfg::SF_STAGE_COLS);
+          const uint32_t sfb_t = sfa_t + 16u;
+          const uint32_t sfa_s = ptx::smem_u32(smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES);
+          const uint32_t sfb_s = ptx::smem_u32(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES);
+          for (int g = 0; g < ns; ++g) {
+            ptx::tc_cp_32x128b_warpx4(sfa_t + 4u * g, ptx::smem_desc(sfa_s + 512u * g, 16u, 128u, ptx::kSwizzleNone));
+#pragma unroll
+            for (int h = 0; h < BN / 128; ++h)
+              ptx::tc_cp_32x128b_warpx4(sfb_t + (uint32_t)(Cfg::SFB_COLS_PER_STEP * g + 4 * h),
+                                        ptx::smem_desc(sfb_s + 2048u * h + 512u * g, 16u, 128u, ptx::kSwizzleNone));
+          }
+          const uint32_t a_s = ptx::smem_u32(smem + Cfg::OFF_A + stage * Cfg::A_BYTES);
+          const uint32_t b_s = ptx::smem_u32(smem + Cfg::OFF_B + stage * Cfg::B_BYTES);
+          for (int g = 0; g < ns; ++g) {
+            const uint64_t adesc = ptx::smem_desc(a_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
+            const uint64_t bdesc = ptx::smem_desc(b_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
+            ptx::tc_mma_nvf4(d_tmem, adesc, bdesc, Cfg::IDESC, sfa_t + 4u * g,
+                             sfb_t + (uint32_t)(Cfg::SFB_COLS_PER_STEP * g), (kt | g) != 0 ? 1u : 0u);
+          }
+          issued = true;
+          ptx::tc_commit(&empty[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        ptx::tc_commit(&tfull[acc]);
+      }
+      if (issued) {
+        // drain: every MMA and copy this thread issued has completed
+        ptx::tc_commit(drain);
+        if (!ptx::mbar_wait(drain, 0, kWaitLimit)) atomicExch(p.err, kErrDrain);
+      }
+    }
+  } else {
+    // epilogue warps: TMEM lane quarter (warp % 4) holds tile rows 32*(warp%4) .. +31
+    const int q = warp & 3;
+    const float alpha = __ldg(p.ts_a) * __ldg(p.ts_b);
+    uint8_t* stage_base = smem + Cfg::OFF_EPI + q * 2 * Cfg::EPI_BUF;
+    int sbuf = 0;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+      const int mt = tile % num_m, nt = tile / num_m;
+      const int acc = Cfg::ACC_BUFS == 2 ? (it & 1) : 0;
+      const uint32_t acc_phase = Cfg::ACC_BUFS == 2 ? ((it >> 1) & 1) : (it & 1);
+      if (!ptx::mbar_wait(&tfull[acc], acc_phase, kWaitLimit)) {
+        atomicExch(p.err, kErrEpilogue);
+        break;
+      }
+      ptx::tc_fence_after();
+      const int row = mt * Cfg::BM + q * 32 + lane;
+      const float rterm = (p.row_vec != nullptr && row < p.M) ? p.outer * __ldg(p.row_vec + row) : 0.f;
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+      constexpr int COLS_PER_STORE = BF16_OUT ? 64 : 32;
+#pragma unroll 1
+      for (int c = 0; c < BN; c += COLS_PER_STORE) {
+        float f[COLS_PER_STORE];
+#pragma unroll
+        for (int h = 0; h < COLS_PER_STORE / 32; ++h) {
+          uint32_t v[32];
+          ptx::tmem_ld32(t_row + (uint32_t)(c + 32 * h), v);
+          ptx::tmem_ld_wait();
+#pragma unroll
+          for (int j = 0; j < 32; ++j) f[32 * h + j] = alpha * __uint_as_float(v[j]);
+        }
+        const int col0 = nt * BN + c;
+        if (p.col_add != nullptr || p.row_vec != nullptr) {
+#pragma unroll
+          for (int j = 0; j < COLS_PER_STORE; ++j) {
+            const int col = col0 + j;
+            if (col < p.N) {
+              if (p.col_add != nullptr) f[j] += __ldg(p.col_add + col);
+              if (p.row_vec != nullptr) f[j] = fmaf(rterm, __ldg(p.col_vec + col), f[j]);
+            }
+          }
+        }
+        uint8_t* sb = stage_base + sbuf * Cfg::EPI_BUF;
+        if (lane == 0) ptx::bulk_wait_read<1>();
+        __syncwarp();
+        uint8_t* srow = sb + lane * 128;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint4 w;
+          if (BF16_OUT) {
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(f[8 * k + 0], f[8 * k + 1]);
+            __nv_bfloat162 b1 = __floats2bfloat162_rn(f[8 * k + 2], f[8 * k + 3]);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * k + 4], f[8 * k + 5]);
+            __nv_bfloat162 b3 = __floats2bfloat162_rn(f[8 * k + 6], f[8 * k + 7]);
+            w = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
+                           *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
+          } else {
+            w = make_uint4(__float_as_uint(f[4 * k]), __float_as_uint(f[4 * k + 1]), __float_as_uint(f[4 * k + 2]),
+                           __float_as_uint(f[4 * k + 3]));
+          }
+          *reinterpret_cast<uint4*>(srow + ((k ^ (lane & 7)) * 16)) = w;
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::tma_store_2d(&tmD, sb, col0, mt * Cfg::BM + q * 32);
+          ptx::bulk_commit();
+        }
+        sbuf ^= 1;
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
+    }
+    if (lane == 0) ptx::bulk_wait<0>();
+    __syncwarp();
+  }
+done:
+  __syncthreads();
+  if (warp == 1) {
+    ptx::tc_fence_after();
+    ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+  }
+}
+
+}  // namespace averis
