@@ -1,0 +1,509 @@
+"""Benchmark: Averis W4A4G4 linear fwd+bwd on the Qwen3-0.6B linears (l = 8192).
+
+One step = forward + backward of the four Qwen3-0.6B-shaped linears (QKV
+1024->4096, o_proj 2048->1024, gate_up 1024->6144, down 3072->1024) at
+l = 8192 tokens (b=4, s=2048): weight quantize, mean-split quantize of X,
+rank-one row, forward GEMM, mean-split quantize of D, rank-one row,
+input-gradient GEMM, weight-gradient GEMM -- all through the C ABI, captured
+in one CUDA graph.  Useful FLOPs per linear: 6 l m n + 5 m n.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line.  Under torchrun each rank runs an independent replica
+(weak scaling: the linears of different batches are independent problems,
+no data-path collective); rank 0 reports the whole-job throughput over the
+max-over-ranks time.  ``--impl reference`` times the CPU float64 oracle on a
+bounded sample of the same workload instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import ctypes
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "Averis W4A4G4 linear fwd+bwd TFLOP/s, % FP4 peak, overhead vs vanilla NVFP4"
+L = workloads.QWEN3_L
+LINEARS = workloads.QWEN3_06B_LINEARS
+FP4_OVER_BF16 = 13.5 / 2.25     # nominal dense FP4 : BF16 tensor-core ratio
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+CPU_SAMPLE_TOKENS = 256
+
+
+def flops_per_step(l=L):
+    return sum(6.0 * l * m * n + 5.0 * m * n for _, m, n in LINEARS)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------ distributed --
+
+def dist_setup():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+        return rank, ws
+    return 0, 1
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(v, ws):
+    if ws == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------- clocks --
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.4)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.out.close()
+
+    def summary(self):
+        rows = []
+        if self.path and os.path.exists(self.path):
+            with open(self.path) as f:
+                for ln in f:
+                    p = [s.strip() for s in ln.split(",")]
+                    if len(p) >= 9:
+                        rows.append(p)
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------- GPU workload --
+
+class Layer:
+    """One linear's inputs, outputs and every intermediate buffer, preallocated."""
+
+    def __init__(self, name, m, n, seed, device):
+        import torch
+        from mean_residual_gemm_col_b300 import capi
+
+        self.name, self.m, self.n = name, m, n
+        self.x, self.w, self.d = workloads.torch_linear_case(seed, L, m, n, spike=workloads.QWEN3_SPIKE,
+                                                             device=device)
+        self.w_n = capi.NVFP4Tensor.empty(m, n, device)
+        self.w_m = capi.NVFP4Tensor.empty(n, m, device)
+        self.state = capi.FwdState.empty(L, m, device)
+        self.y = torch.empty(L, n, dtype=torch.bfloat16, device=device)
+        self.dx = torch.empty(L, m, dtype=torch.bfloat16, device=device)
+        self.dw = torch.empty(m, n, dtype=torch.float32, device=device)
+        self.xq = None   # standalone quantized X / D (same kernels) for the per-kernel timing
+        self.dq = None
+
+
+def quant_weight_into(ly, flags):
+    from mean_residual_gemm_col_b300 import capi
+
+    lib = capi.load()
+    ws = capi.workspace(lib.averis_quantize_workspace_bytes(ly.m, ly.n, flags), ly.w.device, "wq")
+    a, b = ly.w_n.struct(), ly.w_m.struct()
+    capi._check(lib.averis_quantize_weight(capi._ptr(ly.w), ly.m, ly.n, flags, ctypes.byref(a), ctypes.byref(b),
+                                           capi._ptr(ws), ws.numel(), capi._stream(ly.w.device)),
+                "averis_quantize_weight")
+
+
+def run_step(layers, mode):
+    """Enqueue one fwd+bwd step of every layer on the current stream."""
+    from mean_residual_gemm_col_b300 import capi
+
+    split = mode in ("averis", "averis_h16")
+    hf = capi.AVERIS_HADAMARD16 if mode in ("averis_h16", "nvfp4_h16") else 0
+    for ly in layers:
+        quant_weight_into(ly, hf)
+        if split:
+            capi.averis_linear_fwd(ly.x, ly.w_m, capi.AVERIS_MEAN_SPLIT | hf, out_bf16=True, state=ly.state, y=ly.y)
+            capi.averis_linear_bwd(ly.d, ly.state, ly.w_n, capi.AVERIS_MEAN_SPLIT | hf, out_bf16=True, dx=ly.dx,
+                                   dw=ly.dw)
+        else:
+            capi.nvfp4_linear_fwd(ly.x, ly.w_m, hf, out_bf16=True, state=ly.state, y=ly.y)
+            capi.nvfp4_linear_bwd(ly.d, ly.state, ly.w_n, hf, out_bf16=True, dx=ly.dx, dw=ly.dw)
+
+
+def launches_per_step(mode):
+    had = mode in ("averis_h16", "nvfp4_h16")
+    split = mode in ("averis", "averis_h16")
+    q = 4 if had else 3                       # stats, finalize, (amax), quantize
+    per = q + (q + (1 if split else 0) + 1) + (q + (1 if split else 0) + 2)
+    return per * len(LINEARS)
+
+
+def kernel_groups(layers):
+    """Callables that each enqueue one family of launches of a step (for per-kernel timing)."""
+    from mean_residual_gemm_col_b300 import capi
+
+    lib = capi.load()
+
+    def gemms():
+        for ly in layers:
+            st = ly.state
+            capi.averis_gemm(st.x_row, ly.w_m, col_add=None, out_bf16=True, out=ly.y)
+            capi.averis_gemm(ly.dq["row"], ly.w_n, out_bf16=True, out=ly.dx)
+            capi.averis_gemm(st.x_col, ly.dq["col"], row_vec=st.mu_hat, col_vec=ly.dq["mu_hat"], outer=float(L),
+                             out=ly.dw)
+
+    def quants():
+        for ly in layers:
+            for t, rows, cols, q in ((ly.x, L, ly.m, ly.xq), (ly.d, L, ly.n, ly.dq)):
+                ws = capi.workspace(lib.averis_quantize_workspace_bytes(rows, cols, 1), t.device, "kq")
+                ms, rs, cs = q["mu_q"].struct(), q["row"].struct(), q["col"].struct()
+                capi._check(lib.averis_quantize(capi._ptr(t), rows, cols, capi.AVERIS_MEAN_SPLIT, capi._ptr(q["mu"]),
+                                                ctypes.byref(ms), capi._ptr(q["mu_hat"]), ctypes.byref(rs),
+                                                ctypes.byref(cs), capi._ptr(ws), ws.numel(),
+                                                capi._stream(t.device)), "averis_quantize")
+
+    return {"gemm": gemms, "quantize": quants}
+
+
+def gemm_bytes_and_flops(layers):
+    """Algorithmic bytes and flops of the 12 GEMM launches of one step."""
+    from mean_residual_gemm_col_b300 import layout
+
+    def nv(rows, cols):                                   # codes + block scales
+        return rows * layout.cdiv(cols, 16) * 8 + rows * layout.cdiv(cols, 16)
+
+    byts = flops = 0.0
+    for ly in layers:
+        m, n = ly.m, ly.n
+        byts += nv(L, m) + nv(n, m) + 2.0 * L * n        # Y (bf16)
+        byts += nv(L, n) + nv(m, n) + 2.0 * L * m        # dX (bf16)
+        byts += nv(m, L) + nv(n, L) + 4.0 * m * n        # dW (fp32)
+        flops += 6.0 * L * m * n
+    return byts, flops
+
+
+def time_graph(graph, steps, stream):
+    import torch
+
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for _ in range(steps):
+        graph.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+def capture(fn):
+    import torch
+
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def run_ours(args, rank, ws):
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    device = torch.device("cuda", torch.cuda.current_device())
+    capi.load()
+    layers = [Layer(name, m, n, seed=1000 * rank + i, device=device) for i, (name, m, n) in enumerate(LINEARS)]
+    for ly in layers:
+        ly.xq = capi.averis_quantize(ly.x, capi.AVERIS_MEAN_SPLIT)
+        ly.dq = capi.averis_quantize(ly.d, capi.AVERIS_MEAN_SPLIT)
+    modes = ["averis", "nvfp4", "averis_h16"]
+    for mode in modes:       # eager warm-up: kernel attributes, workspaces, first-call setup
+        run_step(layers, mode)
+    torch.cuda.synchronize()
+    if capi.averis_last_device_error() != 0:
+        raise RuntimeError("device-side wait timed out during warm-up")
+    graphs = {mode: capture(lambda mode=mode: run_step(layers, mode)) for mode in modes}
+    groups = kernel_groups(layers)
+    for g in groups.values():
+        g()
+    torch.cuda.synchronize()
+    ggraphs = {k: capture(v) for k, v in groups.items()}
+    stream = torch.cuda.current_stream()
+
+    for _ in range(args.warmup):
+        graphs["averis"].replay()
+    torch.cuda.synchronize()
+
+    # ---- headline: K steps of the Averis fwd+bwd, barrier + sync on both sides
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(ws)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        torch.cuda.nvtx.range_push("averis_timed")
+        ms = time_graph(graphs["averis"], args.steps, stream)
+        torch.cuda.nvtx.range_pop()
+        wall = time.perf_counter() - t0
+        barrier(ws)
+    clocks = clk.summary()
+    ms = max_over_ranks(ms, ws)
+
+    # ---- comparison modes and per-kernel timing (same inputs, same launches)
+    for _ in range(args.warmup):
+        graphs["nvfp4"].replay()
+        graphs["averis_h16"].replay()
+    ms_van = max_over_ranks(time_graph(graphs["nvfp4"], args.steps, stream), ws)
+    ms_had = max_over_ranks(time_graph(graphs["averis_h16"], args.steps, stream), ws)
+    kern = {}
+    for k, g in ggraphs.items():
+        g.replay()
+        kern[k] = time_graph(g, args.steps, stream)
+
+    # ---- end to end through the API with host buffers: H2D inputs, step, D2H outputs
+    host_in = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for ly in layers for t in (ly.x, ly.w, ly.d)]
+    for h, t in host_in:
+        h.copy_(t)
+    host_out = [(torch.empty(t.shape, dtype=t.dtype).pin_memory(), t) for ly in layers for t in (ly.y, ly.dx, ly.dw)]
+    h2d = sum(t.numel() * t.element_size() for _, t in host_in)
+    d2h = sum(t.numel() * t.element_size() for _, t in host_out)
+
+    def e2e_step():
+        for h, t in host_in:
+            t.copy_(h, non_blocking=True)
+        graphs["averis"].replay()
+        for h, t in host_out:
+            h.copy_(t, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    e_steps = max(3, args.steps // 4)
+    barrier(ws)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = max_over_ranks(start.elapsed_time(end) / e_steps, ws)
+    if capi.averis_last_device_error() != 0:
+        raise RuntimeError("device-side wait timed out during the timed region")
+
+    flops = flops_per_step()
+    peaks, src = load_peaks()
+    fp4_peak = peaks["bf16_tflops"] * FP4_OVER_BF16
+    fp4_sus = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"]) * FP4_OVER_BF16
+    value = flops * ws / (ms * 1e-3) / 1e12
+    gb, gf = gemm_bytes_and_flops(layers)
+    n_gemm = 3 * len(LINEARS)
+    g_ms = kern["gemm"] / n_gemm                  # average GEMM launch
+    q_ms = kern["quantize"] / (2 * len(LINEARS))  # average quantize call (3 kernels)
+    q_bytes = sum(3.125 * L * (ly.m + ly.n) for ly in layers) / (2 * len(LINEARS))
+    t_tensor = gf / (fp4_peak * 1e12)
+    t_hbm = gb / (peaks["hbm_gbs"] * 1e9)
+    if t_tensor >= t_hbm:
+        roof = {"bound": "tensor", "achieved": gf / n_gemm / (g_ms * 1e-3) / 1e12, "peak": fp4_peak,
+                "unit": "TFLOP/s"}
+        psrc = f"{src} bf16_tflops x {FP4_OVER_BF16:g} (nominal FP4:BF16 ratio)"
+    else:
+        roof = {"bound": "hbm", "achieved": gb / n_gemm / (g_ms * 1e-3) / 1e9, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s"}
+        psrc = f"{src} hbm_gbs"
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["kernel"] = "gemm_nvfp4_kernel, mean of the 12 GEMM launches of a step"
+    roof["peak_source"] = psrc
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e2m1, fp32 accumulate; bf16 inputs, bf16 Y/dX, fp32 dW)",
+        "data": "synthetic: planted rank-one mean + N(0,1) + 0.1% spikes x30 (seeded torch generator per layer)",
+        "config": {"workload": "Qwen3-0.6B linears (qkv 1024->4096, o_proj 2048->1024, gate_up 1024->6144, "
+                               "down 3072->1024), fwd+bwd", "l": L, "b": 4, "s": 2048,
+                   "parallelism": f"replicas x{ws}", "l2": "step inputs 318 MB > 126 MB L2; no flush",
+                   "cuda_graph": True},
+        "fp4_peak_frac": round(value / ws / fp4_peak, 4),
+        "fp4_peak_tflops": round(fp4_peak, 1),
+        "fp4_peak_sustained_tflops": round(fp4_sus, 1),
+        "overhead_vs_vanilla": round((ms - ms_van) / ms_van, 4),
+        "overhead_h16_vs_vanilla": round((ms_had - ms_van) / ms_van, 4),
+        "ms_per_step_vanilla": round(ms_van, 4),
+        "ms_per_step_averis_h16": round(ms_had, 4),
+        "roofline": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()},
+        "kernels_ms_per_step": {k: round(v, 4) for k, v in kern.items()},
+        "quantize_pass": {"avg_ms": round(q_ms, 4), "algorithmic_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
+                          "hbm_frac": round(q_bytes / (q_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+                          "bytes_per_elem": 3.125},
+        "e2e": {"value": round(flops * ws / (ms_e2e * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(ms_e2e, 3)},
+        "gpu_launches": launches_per_step("averis") * args.steps,
+        "clocks": clocks,
+        "wall_s_timed": round(wall, 4),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
+    return line
+
+
+# --------------------------------------------------------- CPU baseline ----
+
+def cpu_baseline(target_s=10.0):
+    """The oracle, as it stands, on a bounded sample of the workload.
+
+    Sample: the first CPU_SAMPLE_TOKENS tokens of each of the four linears
+    (same m, n), full forward + backward in float64 NumPy, repeated until
+    ``target_s`` seconds of CPU time; throughput in the headline unit.
+    """
+    from oracle import averis as oav
+
+    threads = os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    tok = CPU_SAMPLE_TOKENS
+    total_flops = 0.0
+    t_total = 0.0
+    rep = 0
+    while True:
+        for i, (_, m, n) in enumerate(LINEARS):
+            c = workloads.linear_case(100 + i + 10 * rep, tok, m, n, spike=workloads.QWEN3_SPIKE)
+            x, w, d = (c.x.astype(np.float64), c.w.astype(np.float64), c.d.astype(np.float64))
+            t0 = time.perf_counter()
+            oav.linear_fwd_bwd(x, w, d)
+            t_total += time.perf_counter() - t0
+            total_flops += 6.0 * tok * m * n + 5.0 * m * n
+        rep += 1
+        if t_total >= target_s:
+            break
+    return {"value": round(total_flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+            "threads": threads, "kind": "oracle",
+            "sample": f"{rep} x ({tok} of {L} tokens of each of the 4 linears, fwd+bwd), float64 NumPy, "
+                      f"{t_total:.1f} s"}
+
+
+def run_reference(args, rank, ws):
+    """The CPU oracle as the reference arm: each step is one bounded sample of the workload."""
+    if rank != 0:
+        return None
+    for _ in range(args.warmup):
+        cpu_baseline(target_s=0.0)
+    per = [cpu_baseline(target_s=0.0) for _ in range(args.steps)]
+    v = statistics.median(c["value"] for c in per)
+    step_flops = flops_per_step(CPU_SAMPLE_TOKENS)
+    ms = step_flops / (v * 1e12) * 1e3
+    cb = {"value": v, "unit": "TFLOP/s", "cores": per[-1]["cores"], "kind": "oracle",
+          "sample": f"{CPU_SAMPLE_TOKENS} of {L} tokens of each of the 4 linears per step, fwd+bwd, float64 NumPy"}
+    return {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (NumPy PCG64, same recipe)",
+        "config": {"workload": "Qwen3-0.6B linears (qkv 1024->4096, o_proj 2048->1024, gate_up 1024->6144, "
+                               "down 3072->1024), fwd+bwd; bounded sample", "l": L},
+        "cpu_baseline": cb,
+        "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, ws = dist_setup()
+    if args.impl == "reference":
+        line = run_reference(args, rank, ws)
+    else:
+        line = run_ours(args, rank, ws)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

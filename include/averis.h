@@ -155,7 +155,8 @@ averis_status averis_rank1(const averis_nvfp4* mu_q, const averis_nvfp4* w, floa
  * averis_gemm -- block-scaled NVFP4 GEMM on the tcgen05 tensor cores with the
  * Averis epilogue:
  *   out[i][j] = s_a s_b sum_k a[i][k] b[j][k] + col_add[j] + outer_scale * row_vec[i] * col_vec[j]
- *  a        NVFP4 [M, K];  b  NVFP4 [N, K] (both blocked along K).
+ *  a        NVFP4 [M, K];  b  NVFP4 [N, K] (both blocked along K; K >= 1 need not
+ *           be a multiple of 16: the last block's padding is zero in both).
  *  col_add  device [N] or NULL (the broadcast mean term of Y and dX).
  *  row_vec, col_vec  device [M], [N] or both NULL (the l mu_X^T mu_D term of dW).
  *  out      device [M, ldo] binary32, or bf16 with AVERIS_OUT_BF16; ldo >= N,

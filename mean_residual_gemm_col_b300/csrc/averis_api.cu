@@ -227,7 +227,8 @@ averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const floa
                         const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s) {
   if (a == nullptr || b == nullptr || out == nullptr) return AVERIS_ERR_INVALID_ARG;
   const int64_t M = a->rows, N = b->rows, K = a->cols;
-  if (M < 1 || N < 1 || K < 16 || K % 16 != 0 || b->cols != K) return AVERIS_ERR_INVALID_ARG;
+  // K may be ragged (the token axis of dW): codes and scales are zero-padded to 64
+  if (M < 1 || N < 1 || K < 1 || b->cols != K) return AVERIS_ERR_INVALID_ARG;
   if (M > (int64_t)1 << 30 || N > (int64_t)1 << 30 || K > (int64_t)1 << 30) return AVERIS_ERR_INVALID_ARG;
   if (!nvfp4_ok(a, M, K) || !nvfp4_ok(b, N, K)) return AVERIS_ERR_INVALID_ARG;
   const bool bf16 = (flags & AVERIS_OUT_BF16) != 0;
