@@ -212,6 +212,35 @@ averis_status nvfp4_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n,
                                unsigned flags, void* dx, float* dw,
                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/*
+ * averis_quantize_noalloc -- averis_quantize without a caller-supplied
+ * workspace.  The method has no counterpart of this call: it exists for
+ * callers that cannot allocate device memory, such as plugin hosts that hand
+ * an operator only its input and output buffers and own every other
+ * allocation, or code that must not call cudaMalloc because it implicitly
+ * synchronizes the device.
+ *
+ * Arguments, outputs and results are those of averis_quantize (same kernels,
+ * same bits).  The scratch is one file-scope device array of
+ * AVERIS_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.  The call allocates nothing.
+ *  - The first call on a device looks up that array's device address (once per
+ *    device, with the device current); make that first call before any stream
+ *    capture.
+ *  - Every call shares the one array, and it keeps the previous call's
+ *    contents; the kernels clear the part that must start at zero.  Calls
+ *    whose work overlaps on the GPU (other streams, other host threads) race
+ *    on the array and give wrong results: order them on one stream.
+ *  - Sizes whose scratch need, averis_quantize_workspace_bytes(rows, cols, flags),
+ *    exceeds AVERIS_NOALLOC_SCRATCH_BYTES return AVERIS_ERR_WORKSPACE_TOO_SMALL
+ *    and enqueue nothing.
+ */
+#define AVERIS_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+averis_status averis_quantize_noalloc(const void* x, int64_t rows, int64_t cols, unsigned flags,
+                                      float* mu, const averis_nvfp4* mu_q, float* mu_hat,
+                                      const averis_nvfp4* out_row, const averis_nvfp4* out_col,
+                                      cudaStream_t stream);
+
 /* Human-readable name of a status. */
 const char* averis_status_string(averis_status status);
 

@@ -33,7 +33,7 @@ EXPORTS = (
     "averis_quantize_workspace_bytes", "averis_quantize", "averis_quantize_weight", "averis_rank1",
     "averis_gemm", "averis_linear_fwd_workspace_bytes", "averis_linear_bwd_workspace_bytes",
     "averis_linear_fwd", "averis_linear_bwd", "nvfp4_linear_fwd", "nvfp4_linear_bwd",
-    "averis_status_string", "averis_last_device_error", "averis_version",
+    "averis_status_string", "averis_last_device_error", "averis_version", "averis_quantize_noalloc",
 )
 
 
@@ -77,6 +77,7 @@ def _declare(lib):
         "averis_status_string": (ctypes.c_char_p, [I]),
         "averis_last_device_error": (I, [P, ctypes.POINTER(I)]),
         "averis_version": (I, []),
+        "averis_quantize_noalloc": (I, [P, I64, I64, U, P, NP, P, NP, NP, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -224,6 +225,35 @@ def averis_quantize(x, flags: int = AVERIS_MEAN_SPLIT, want_row=True, want_col=T
                              ctypes.byref(rs) if rs else None, ctypes.byref(cs) if cs else None,
                              _ptr(ws), ws.numel(), _stream(dev))
     _check(st, "averis_quantize")
+    return dict(mu=mu, mu_q=mu_q, mu_hat=mu_hat, row=row, col=col)
+
+
+def averis_quantize_noalloc(x, flags: int = AVERIS_MEAN_SPLIT, want_row=True, want_col=True):
+    """``averis_quantize`` through the entry point that takes no workspace.
+
+    For callers that cannot allocate device scratch: the library's own
+    file-scope scratch array is used instead (calls on one stream only; see
+    include/averis.h).  Outputs are allocated here, as in ``averis_quantize``.
+    """
+    import torch
+
+    lib = load()
+    _check_bf16(x, "x")
+    R, C = x.shape
+    dev = x.device
+    split = bool(flags & AVERIS_MEAN_SPLIT)
+    row = NVFP4Tensor.empty(R, C, dev) if want_row else None
+    col = NVFP4Tensor.empty(C, R, dev) if want_col else None
+    mu = torch.zeros(C, dtype=torch.float32, device=dev) if split else None
+    mu_hat = torch.zeros(C, dtype=torch.float32, device=dev) if split else None
+    mu_q = NVFP4Tensor.empty(1, C, dev) if split else None
+    rs = row.struct() if row else None
+    cs = col.struct() if col else None
+    ms = mu_q.struct() if mu_q else None
+    st = lib.averis_quantize_noalloc(_ptr(x), R, C, flags, _ptr(mu), ctypes.byref(ms) if ms else None,
+                                     _ptr(mu_hat), ctypes.byref(rs) if rs else None,
+                                     ctypes.byref(cs) if cs else None, _stream(dev))
+    _check(st, "averis_quantize_noalloc")
     return dict(mu=mu, mu_q=mu_q, mu_hat=mu_hat, row=row, col=col)
 
 

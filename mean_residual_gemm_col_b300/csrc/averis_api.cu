@@ -490,3 +490,44 @@ averis_status averis_last_device_error(cudaStream_t stream, int* where) {
 int averis_version(void) { return 100; }
 
 }  // extern "C"
+
+// ===================================================== allocation-free call ==
+
+// Scratch of averis_quantize_noalloc: one array per device, alive until the
+// process exits.  Host code must not pass &g_noalloc_scratch to a kernel (it
+// names a host-side shadow); the device address comes from
+// cudaGetSymbolAddress, looked up once per device.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[AVERIS_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+
+void* g_noalloc_addr[kMaxDevices] = {};
+
+averis_status noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return AVERIS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return AVERIS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (g_noalloc_addr[dev] == nullptr) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) return AVERIS_ERR_CUDA;
+    g_noalloc_addr[dev] = addr;
+  }
+  *out = g_noalloc_addr[dev];
+  return AVERIS_OK;
+}
+
+}  // namespace
+
+extern "C" averis_status averis_quantize_noalloc(const void* x, int64_t rows, int64_t cols, unsigned flags,
+                                                 float* mu, const averis_nvfp4* mu_q, float* mu_hat,
+                                                 const averis_nvfp4* out_row, const averis_nvfp4* out_col,
+                                                 cudaStream_t stream) {
+  if (rows < 1 || cols < 1) return AVERIS_ERR_INVALID_ARG;
+  if (quant_ws_bytes(rows, cols) > AVERIS_NOALLOC_SCRATCH_BYTES) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
+  void* scratch = nullptr;
+  averis_status st = noalloc_scratch(&scratch);
+  if (st != AVERIS_OK) return st;
+  return quantize_impl(x, rows, cols, flags, mu, mu_q, mu_hat, out_row, out_col, scratch,
+                       AVERIS_NOALLOC_SCRATCH_BYTES, stream);
+}
