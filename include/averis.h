@@ -34,6 +34,11 @@
  *    averis_last_device_error().
  *  - bf16 inputs are row-major and 16-byte aligned; every device pointer must
  *    be 16-byte aligned (256-byte for workspaces).
+ *  - Workspaces: the first AVERIS_WORKSPACE_CTRL_BYTES bytes of every
+ *    workspace are a control block (tickets and running maxima) that must be
+ *    zero before the workspace is first used; every call leaves it zero
+ *    again, so zero-fill a workspace once when allocating it.  The rest is
+ *    scratch.
  *  - Calls that share a workspace or an output must not overlap in time.
  *  - Sizes: cols of every NVFP4 tensor and the m, n of a linear layer must be
  *    multiples of 16; the token count l may be any value >= 1 (a partial last
@@ -58,6 +63,9 @@ typedef enum {
   AVERIS_ERR_WORKSPACE_TOO_SMALL = 4,
   AVERIS_ERR_TIMEOUT = 5             /* a device-side wait gave up (see averis_last_device_error) */
 } averis_status;
+
+/* Size of the control block at the head of every workspace (zero at rest). */
+#define AVERIS_WORKSPACE_CTRL_BYTES 4352
 
 /* flags */
 #define AVERIS_MEAN_SPLIT 1u  /* subtract the column mean (Averis); clear = vanilla NVFP4 */

@@ -182,13 +182,17 @@ _ws_cache = {}
 
 
 def workspace(nbytes: int, device, key: str = "default"):
-    """A cached device scratch buffer of at least ``nbytes`` (256-byte aligned)."""
+    """A cached device workspace of at least ``nbytes`` (256-byte aligned).
+
+    Allocated zero-filled: the library requires the control block at the head
+    of a workspace to be zero before its first use and leaves it zero.
+    """
     import torch
 
     k = (str(device), key)
     buf = _ws_cache.get(k)
     if buf is None or buf.numel() < nbytes:
-        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        buf = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
         _ws_cache[k] = buf
     return buf
 

@@ -18,7 +18,7 @@ namespace {
 using namespace averis;
 
 constexpr int kMaxDevices = 64;
-constexpr int kStatsTargetCtas = 1184;  // row-block count target of the stats pass
+constexpr int kStatsTargetCtas = 592;  // CTA count target of the stats pass (4 per SM of a B300)
 
 __device__ int g_device_error = 0;
 
@@ -101,25 +101,50 @@ averis_status launch_status() { return cudaGetLastError() == cudaSuccess ? AVERI
 // ------------------------------------------------------------ geometry --
 
 struct StatsGeom {
-  int strips, nrb;
+  int gx, nstrips, nrb;
   int64_t rows_per;
 };
 
+// Stats-pass grid: 64-column strips, at most kMaxStripGroups strip groups,
+// and enough row blocks for about kStatsTargetCtas CTAs in all.
 StatsGeom stats_geom(int64_t R, int64_t C) {
   StatsGeom g;
-  g.strips = (int)cdiv(C, 256);
-  int64_t nrb = cdiv(kStatsTargetCtas, g.strips);
-  nrb = std::max<int64_t>(1, std::min<int64_t>(nrb, cdiv(R, 64)));
+  g.nstrips = (int)cdiv(C, 64);
+  g.gx = std::min(g.nstrips, (int)kMaxStripGroups);
+  int64_t nrb = cdiv(kStatsTargetCtas, g.gx);
+  nrb = std::max<int64_t>(1, std::min<int64_t>(nrb, cdiv(R, 128)));
   int64_t rp = cdiv(R, nrb);
-  rp = cdiv(rp, 32) * 32;
+  rp = cdiv(rp, 128) * 128;
   g.rows_per = rp;
   g.nrb = (int)cdiv(R, rp);
   return g;
 }
 
+constexpr size_t kCtrlBytes = ((size_t)kCtrlWords * sizeof(unsigned) + 255) & ~size_t(255);
+static_assert(kCtrlBytes == AVERIS_WORKSPACE_CTRL_BYTES, "control block size is part of the ABI");
+
 size_t quant_ws_bytes(int64_t R, int64_t C) {
   const StatsGeom g = stats_geom(R, C);
-  return align256(kCtrlWords * sizeof(unsigned)) + align256((size_t)g.nrb * (size_t)C * sizeof(ColPartial));
+  return kCtrlBytes + align256((size_t)g.nrb * (size_t)C * sizeof(ColPartial));
+}
+
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes; it waits (griddepcontrol.wait)
+// before touching anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
 bool nvfp4_ok(const averis_nvfp4* t, int64_t rows, int64_t cols) {
@@ -150,31 +175,29 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
 
   uint8_t* w = static_cast<uint8_t*>(ws);
   unsigned* ctrl = reinterpret_cast<unsigned*>(w);
-  ColPartial* part = reinterpret_cast<ColPartial*>(w + align256(kCtrlWords * sizeof(unsigned)));
+  ColPartial* part = reinterpret_cast<ColPartial*>(w + kCtrlBytes);
   const StatsGeom g = stats_geom(R, C);
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
 
-  colstats_partial_kernel<<<dim3(g.strips, g.nrb), 256, 0, s>>>(xb, R, C, g.rows_per, part, ctrl);
-  if ((st = launch_status()) != AVERIS_OK) return st;
-
-  FinalizeParams fp{};
-  fp.part = part;
-  fp.nrb = g.nrb;
-  fp.R = R;
-  fp.C = C;
-  fp.split = split ? 1 : 0;
-  fp.hadamard = had ? 1 : 0;
-  fp.mu = mu;
-  fp.ctrl = ctrl;
+  StatsParams sp{};
+  sp.x = xb;
+  sp.R = R;
+  sp.C = C;
+  sp.rows_per = g.rows_per;
+  sp.nstrips = g.nstrips;
+  sp.part = part;
+  sp.ctrl = ctrl;
+  sp.split = split ? 1 : 0;
+  sp.hadamard = had ? 1 : 0;
+  sp.mu = mu;
   if (split) {
-    fp.mu_codes = mu_q->codes;
-    fp.mu_scales = mu_q->scales;
-    fp.mu_ts = mu_q->tensor_scale;
-    fp.mu_hat = mu_hat;
+    sp.mu_codes = mu_q->codes;
+    sp.mu_scales = mu_q->scales;
+    sp.mu_ts = mu_q->tensor_scale;
+    sp.mu_hat = mu_hat;
   }
-  fp.kc = cdiv(C, 64);
-  colstats_finalize_kernel<<<(unsigned)cdiv(C, 256), 256, 0, s>>>(fp);
-  if ((st = launch_status()) != AVERIS_OK) return st;
+  sp.kc = cdiv(C, 64);
+  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), 0, s, sp) != cudaSuccess) return AVERIS_ERR_CUDA;
 
   if (out_row == nullptr && out_col == nullptr) return AVERIS_OK;
   QuantParams qp{};
@@ -202,12 +225,11 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   qp.tiles_c = (int)cdiv(C, kQTile);
   const int ntiles = qp.tiles_r * qp.tiles_c;
   const int grid = (int)std::min<int64_t>(ntiles, 2 * (int64_t)dev->sms);
-  if (had) {
-    split_quant_kernel<true><<<grid, kQThreads, kQSmem, s>>>(qp);
-    if ((st = launch_status()) != AVERIS_OK) return st;
-  }
-  split_quant_kernel<false><<<grid, kQThreads, kQSmem, s>>>(qp);
-  return launch_status();
+  if (had && launch_pdl(split_quant_kernel<true>, dim3(grid), dim3(kQThreads), kQSmem, s, qp) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (launch_pdl(split_quant_kernel<false>, dim3(grid), dim3(kQThreads), kQSmem, s, qp) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  return AVERIS_OK;
 }
 
 // ----------------------------------------------------------------- GEMM --
@@ -285,10 +307,12 @@ averis_status rank1_impl(const averis_nvfp4* mu_q, const averis_nvfp4* w, float*
   DeviceInfo* dev = nullptr;
   averis_status st = device_info(&dev);
   if (st != AVERIS_OK) return st;
-  rank1_gemv_kernel<<<(unsigned)cdiv(N, 8), 256, 0, s>>>(mu_q->codes, mu_q->scales, mu_q->tensor_scale, w->codes,
-                                                         w->scales, w->tensor_scale, averis_nvfp4_ld(K), N, K,
-                                                         cdiv(K, 64), out);
-  return launch_status();
+  if (launch_pdl(rank1_gemv_kernel, dim3((unsigned)cdiv(N, 8)), dim3(256), 0, s, (const uint8_t*)mu_q->codes,
+                 (const uint8_t*)mu_q->scales, (const float*)mu_q->tensor_scale, (const uint8_t*)w->codes,
+                 (const uint8_t*)w->scales, (const float*)w->tensor_scale, averis_nvfp4_ld(K), N, K, cdiv(K, 64),
+                 out) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  return AVERIS_OK;
 }
 
 // --------------------------------------------------------------- layers --

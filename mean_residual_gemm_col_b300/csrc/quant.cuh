@@ -1,10 +1,11 @@
 // Mean-split NVFP4 quantize pass and the rank-one GEMV.
 //
-// Pass 1  colstats_partial : per (row block, column) compensated sum, max, min
-//                            of the bf16 input (one coalesced read).
-// Pass 1b colstats_finalize: column mean mu (binary32), the residual's exact
-//                            maximum magnitude, and -- in the last block to
-//                            finish -- the NVFP4 quantization of mu itself.
+// Pass 1  colstats         : per column compensated sum, max and min of the
+//                            bf16 input in one coalesced read; the last CTAs
+//                            to finish combine them into the mean mu
+//                            (binary32), the residual's exact maximum
+//                            magnitude, the tensor scales, and the NVFP4
+//                            quantization of mu itself.
 // Pass 2  split_quant      : r = fl32(x - mu) (optionally rotated by H16/4),
 //                            NVFP4 along the columns AND along the rows, both
 //                            layouts written in one read of the tile.
@@ -27,8 +28,22 @@
 
 namespace averis {
 
-// control words at the head of a quantize workspace
-enum : int { kCtrlTicket = 0, kCtrlAmaxRow = 1, kCtrlAmaxCol = 2, kCtrlAmaxMu = 3, kCtrlWords = 64 };
+// Control block at the head of every quantize workspace.  Every word below
+// kCtrlScaleRow is zero at rest: the kernel that counts on a ticket or
+// accumulates a maximum resets it before it finishes, so a workspace that
+// starts zeroed stays usable for any later call without a memset.
+enum : int {
+  kCtrlTicket = 0,       // stats pass: strips finished
+  kCtrlAmaxRow = 1,      // residual max magnitude, layout blocked along columns (float bits)
+  kCtrlAmaxCol = 2,      // same, layout blocked along rows
+  kCtrlAmaxMu = 3,       // max |mu|
+  kCtrlAmaxTicket = 4,   // rotated-amax pass: CTAs finished
+  kCtrlScaleRow = 8,     // tensor scales handed to the quantize pass (written every call)
+  kCtrlScaleCol = 9,
+  kCtrlStrip = 64,       // per-strip-group tickets of the stats pass
+  kMaxStripGroups = 1024,
+  kCtrlWords = kCtrlStrip + kMaxStripGroups
+};
 
 struct ColPartial {
   float s_hi, s_lo, mx, mn;
@@ -43,87 +58,12 @@ __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t k, int64_t kc
   return ((r >> 7) * kc + (k >> 2)) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5) + (k & 3);
 }
 
-// ------------------------------------------------------------ pass 1 ----
-
-// grid (strips of 256 columns, row blocks); 256 threads.  Thread: 8 columns,
-// rows warp, warp+8, ... of its row block, four rows per step.  The four rows
-// are summed pairwise and the step sum is added with Kahan compensation.
-__global__ void __launch_bounds__(256) colstats_partial_kernel(const __nv_bfloat16* __restrict__ x, int64_t R,
-                                                               int64_t C, int64_t rows_per,
-                                                               ColPartial* __restrict__ part,
-                                                               unsigned* __restrict__ ctrl) {
-  __shared__ double s_sum[8][256];
-  __shared__ float s_mx[8][256], s_mn[8][256];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < kCtrlWords) ctrl[threadIdx.x] = 0u;
-
-  const int64_t c0 = (int64_t)blockIdx.x * 256 + lane * 8;
-  const bool col_ok = c0 < C;
-  const int64_t rb0 = (int64_t)blockIdx.y * rows_per;
-  const int64_t rb1 = min(R, rb0 + rows_per);
-
-  float s[8], c[8], mx[8], mn[8];
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    s[e] = 0.f;
-    c[e] = 0.f;
-    mx[e] = -FLT_MAX;
-    mn[e] = FLT_MAX;
-  }
-  if (col_ok) {
-    for (int64_t r = rb0 + warp; r < rb1; r += 32) {
-      uint4 v[4];
-      bool ok[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int64_t rr = r + 8 * j;
-        ok[j] = rr < rb1;
-        v[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(x + rr * C + c0)) : make_uint4(0, 0, 0, 0);
-      }
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        float a[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t w = (e >> 1) == 0 ? v[j].x : (e >> 1) == 1 ? v[j].y : (e >> 1) == 2 ? v[j].z : v[j].w;
-          a[j] = (e & 1) ? bf16hi(w) : bf16lo(w);
-          if (ok[j]) {
-            mx[e] = fmaxf(mx[e], a[j]);
-            mn[e] = fminf(mn[e], a[j]);
-          }
-        }
-        const float t = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
-        const float y = __fsub_rn(t, c[e]);
-        const float tt = __fadd_rn(s[e], y);
-        c[e] = __fsub_rn(__fsub_rn(tt, s[e]), y);
-        s[e] = tt;
-      }
-    }
-  }
-#pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    s_sum[warp][lane * 8 + e] = (double)s[e] - (double)c[e];
-    s_mx[warp][lane * 8 + e] = mx[e];
-    s_mn[warp][lane * 8 + e] = mn[e];
-  }
-  __syncthreads();
-  const int64_t col = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  if (col < C) {
-    double acc = 0.0;
-    float m1 = -FLT_MAX, m2 = FLT_MAX;
-#pragma unroll
-    for (int w = 0; w < 8; ++w) {
-      acc += s_sum[w][threadIdx.x];
-      m1 = fmaxf(m1, s_mx[w][threadIdx.x]);
-      m2 = fminf(m2, s_mn[w][threadIdx.x]);
-    }
-    ColPartial p;
-    p.s_hi = (float)acc;
-    p.s_lo = (float)(acc - (double)p.s_hi);
-    p.mx = m1;
-    p.mn = m2;
-    part[(int64_t)blockIdx.y * C + col] = p;
-  }
+// Programmatic dependent launch: wait until the previous kernel of the stream
+// has completed and its writes are visible, then let the next kernel start
+// launching (its own wait keeps it from reading what this one writes).
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Block-wide max of non-negative floats (blockDim 256).
@@ -198,53 +138,186 @@ __device__ __forceinline__ float e2m1_val(uint32_t c4) {
   return (c4 & 8u) ? -v : v;
 }
 
-struct FinalizeParams {
-  const ColPartial* part;
-  int nrb;
+// ------------------------------------------------------------ pass 1 ----
+
+struct StatsParams {
+  const __nv_bfloat16* x;
   int64_t R, C;
-  int split;     // mean split on
-  int hadamard;  // rotation on (amax of the residual comes from the amax pass)
-  float* mu;     // [C] out (split)
+  int64_t rows_per;   // rows per CTA row block (multiple of 128)
+  int nstrips;        // ceil(C / 64) column strips of 64
+  ColPartial* part;   // [gridDim.y][C] per-row-block partials
   unsigned* ctrl;
+  int split;          // mean split on
+  int hadamard;       // rotation on (the rotated residual's maximum comes from the amax pass)
+  float* mu;          // [C] out (split)
   // quantized mean (split): [1, C]
   uint8_t* mu_codes;
   uint8_t* mu_scales;
   float* mu_ts;
-  float* mu_hat;  // [C] dequantized, unrotated
-  int64_t kc;     // ceil(C/64)
+  float* mu_hat;      // [C] dequantized, unrotated
+  int64_t kc;         // ceil(C / 64)
 };
 
-// grid ceil(C/256) x 256 threads; thread = column.
-__global__ void __launch_bounds__(256) colstats_finalize_kernel(FinalizeParams p) {
+// Column statistics in one pass over X, with the combine fused in.
+//
+// grid (strip groups, row blocks), 256 threads.  CTA (g, b) reads rows
+// [b*rows_per, (b+1)*rows_per) of the 64-column strips g, g+gridDim.x, ...:
+// thread t owns 8 adjacent columns (16-byte loads) of rows t/8, t/8+32, ...,
+// keeps a Kahan-compensated binary32 sum plus max and min per column, and the
+// 32 row lanes are combined in float64 in a fixed order.  The last CTA of a
+// strip group to finish (ticket) combines the row-block partials of its
+// strips in row-block order -- the result does not depend on which CTA is
+// last -- giving mu_j = fl32(S_j / R) and the residual's exact maximum
+// magnitude max(|fl32(max_j - mu_j)|, |fl32(min_j - mu_j)|) (binary32
+// subtraction is monotone).  The last strip group overall turns the maxima
+// into the two tensor scales and quantizes mu as a [1, C] NVFP4 row.
+__global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
+  __shared__ double s_sum[8][64];
+  __shared__ float s_mx[8][64], s_mn[8][64];
   __shared__ float red[8];
   __shared__ int s_last;
-  const int64_t j = (int64_t)blockIdx.x * 256 + threadIdx.x;
-  float a_col = 0.f, a_mu = 0.f;
-  if (j < p.C) {
-    double s = 0.0;
-    float mx = -FLT_MAX, mn = FLT_MAX;
-    for (int rb = 0; rb < p.nrb; ++rb) {
-      const ColPartial q = p.part[(int64_t)rb * p.C + j];
-      s += (double)q.s_hi + (double)q.s_lo;
-      mx = fmaxf(mx, q.mx);
-      mn = fminf(mn, q.mn);
+  pdl_wait_and_release();
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g8 = tid & 7;     // 8-column group inside the strip
+  const int rl = tid >> 3;    // row lane 0..31
+  const int64_t rb0 = (int64_t)blockIdx.y * p.rows_per;
+  const int64_t rb1 = min(p.R, rb0 + p.rows_per);
+
+  for (int strip = blockIdx.x; strip < p.nstrips; strip += gridDim.x) {
+    const int64_t c0 = (int64_t)strip * 64 + 8 * g8;
+    float s[8], c[8], mx[8], mn[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      s[e] = 0.f;
+      c[e] = 0.f;
+      mx[e] = -FLT_MAX;
+      mn[e] = FLT_MAX;
     }
-    if (p.split) {
-      const float mu = (float)(s / (double)p.R);
-      p.mu[j] = mu;
-      a_col = fmaxf(fabsf(__fsub_rn(mx, mu)), fabsf(__fsub_rn(mn, mu)));
-      a_mu = fabsf(mu);
-    } else {
-      a_col = fmaxf(fabsf(mx), fabsf(mn));
+    if (c0 < p.C) {
+      const __nv_bfloat16* base = p.x + c0;
+      for (int64_t r = rb0 + rl; r < rb1; r += 128) {
+        uint4 v[4];
+        bool ok[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int64_t rr = r + 32 * j;
+          ok[j] = rr < rb1;
+          v[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(base + rr * p.C)) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float a[4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint32_t w = (e >> 1) == 0 ? v[j].x : (e >> 1) == 1 ? v[j].y : (e >> 1) == 2 ? v[j].z : v[j].w;
+            a[j] = (e & 1) ? bf16hi(w) : bf16lo(w);
+            if (ok[j]) {
+              mx[e] = fmaxf(mx[e], a[j]);
+              mn[e] = fminf(mn[e], a[j]);
+            }
+          }
+          // rows that are out of range contribute an exact 0 to the sum
+          const float t = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
+          const float y = __fsub_rn(t, c[e]);
+          const float tt = __fadd_rn(s[e], y);
+          c[e] = __fsub_rn(__fsub_rn(tt, s[e]), y);
+          s[e] = tt;
+        }
+      }
     }
+    // combine the 4 row lanes of this warp that share the columns (lanes differ by 8, 16)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      double d = (double)s[e] - (double)c[e];
+      d += __shfl_xor_sync(0xffffffffu, d, 8);
+      d += __shfl_xor_sync(0xffffffffu, d, 16);
+      float m1 = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 16));
+      float m2 = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], 8));
+      m2 = fminf(m2, __shfl_xor_sync(0xffffffffu, m2, 16));
+      if (lane < 8) {
+        s_sum[warp][8 * lane + e] = d;
+        s_mx[warp][8 * lane + e] = m1;
+        s_mn[warp][8 * lane + e] = m2;
+      }
+    }
+    __syncthreads();
+    if (tid < 64) {
+      const int64_t col = (int64_t)strip * 64 + tid;
+      double acc = 0.0;
+      float m1 = -FLT_MAX, m2 = FLT_MAX;
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        acc += s_sum[w][tid];
+        m1 = fmaxf(m1, s_mx[w][tid]);
+        m2 = fminf(m2, s_mn[w][tid]);
+      }
+      if (col < p.C) {
+        ColPartial q;
+        q.s_hi = (float)acc;
+        q.s_lo = (float)(acc - (double)q.s_hi);
+        q.mx = m1;
+        q.mn = m2;
+        *reinterpret_cast<float4*>(p.part + (int64_t)blockIdx.y * p.C + col) = make_float4(q.s_hi, q.s_lo, q.mx, q.mn);
+      }
+    }
+    __syncthreads();
   }
-  __threadfence();  // publish mu before this block takes its ticket
-  a_col = block_max256(a_col, red);
+
+  // ---- last row block of this strip group combines the partials
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned t = atomicAdd(&p.ctrl[kCtrlStrip + blockIdx.x], 1u);
+    s_last = (t == gridDim.y - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  float a_res = 0.f, a_mu = 0.f;
+  const int nrb = (int)gridDim.y;
+  for (int strip = blockIdx.x; strip < p.nstrips; strip += gridDim.x) {
+    const int cl = tid & 63, part = tid >> 6;
+    const int64_t col = (int64_t)strip * 64 + cl;
+    double acc = 0.0;
+    float m1 = -FLT_MAX, m2 = FLT_MAX;
+    if (col < p.C) {
+      for (int rb = part; rb < nrb; rb += 4) {
+        const float4 q = __ldcg(reinterpret_cast<const float4*>(p.part + (int64_t)rb * p.C + col));
+        acc += (double)q.x + (double)q.y;
+        m1 = fmaxf(m1, q.z);
+        m2 = fminf(m2, q.w);
+      }
+    }
+    s_sum[part][cl] = acc;
+    s_mx[part][cl] = m1;
+    s_mn[part][cl] = m2;
+    __syncthreads();
+    if (tid < 64 && col < p.C) {
+      const double S = ((s_sum[0][cl] + s_sum[1][cl]) + s_sum[2][cl]) + s_sum[3][cl];
+      const float M1 = fmaxf(fmaxf(s_mx[0][cl], s_mx[1][cl]), fmaxf(s_mx[2][cl], s_mx[3][cl]));
+      const float M2 = fminf(fminf(s_mn[0][cl], s_mn[1][cl]), fminf(s_mn[2][cl], s_mn[3][cl]));
+      if (p.split) {
+        const float mu = (float)(S / (double)p.R);
+        p.mu[col] = mu;
+        a_res = fmaxf(a_res, fmaxf(fabsf(__fsub_rn(M1, mu)), fabsf(__fsub_rn(M2, mu))));
+        a_mu = fmaxf(a_mu, fabsf(mu));
+      } else {
+        a_res = fmaxf(a_res, fmaxf(fabsf(M1), fabsf(M2)));
+      }
+    }
+    __syncthreads();
+  }
+  if (tid == 0) p.ctrl[kCtrlStrip + blockIdx.x] = 0u;  // every row block has arrived: reset for the next call
+  a_res = block_max256(a_res, red);
   a_mu = block_max256(a_mu, red);
-  if (threadIdx.x == 0) {
+  __threadfence();  // publish mu before taking the overall ticket
+  if (tid == 0) {
     if (!p.hadamard) {
-      atomicMax(&p.ctrl[kCtrlAmaxRow], __float_as_uint(a_col));
-      atomicMax(&p.ctrl[kCtrlAmaxCol], __float_as_uint(a_col));
+      atomicMax(&p.ctrl[kCtrlAmaxRow], __float_as_uint(a_res));
+      atomicMax(&p.ctrl[kCtrlAmaxCol], __float_as_uint(a_res));
     }
     atomicMax(&p.ctrl[kCtrlAmaxMu], __float_as_uint(a_mu));
     __threadfence();
@@ -252,19 +325,33 @@ __global__ void __launch_bounds__(256) colstats_finalize_kernel(FinalizeParams p
     s_last = (t == gridDim.x - 1);
   }
   __syncthreads();
-  if (!s_last || !p.split) return;
+  if (!s_last) return;
   __threadfence();
 
-  // Last block: quantize mu along C as one row ([1, C]).  Under the
-  // Hadamard variant mu is rotated block-wise first, and mu_hat is the
-  // dequantized mean rotated back (H16/4 is its own inverse).
+  // ---- last strip group overall: tensor scales, reset, quantize mu
+  __shared__ float s_amax_mu;
+  if (tid == 0) {
+    if (!p.hadamard) {
+      const float ar = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxRow], 0u));
+      const float ac = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxCol], 0u));
+      p.ctrl[kCtrlScaleRow] = __float_as_uint(tensor_scale_of(ar));
+      p.ctrl[kCtrlScaleCol] = __float_as_uint(tensor_scale_of(ac));
+    }
+    s_amax_mu = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxMu], 0u));
+    p.ctrl[kCtrlTicket] = 0u;
+    __threadfence();
+  }
+  __syncthreads();
+  if (!p.split) return;
+
+  // Quantize mu along C as one row ([1, C]).  Under the Hadamard variant mu
+  // is rotated block-wise first, and mu_hat is the dequantized mean rotated
+  // back (H16/4 is its own inverse).
   const int64_t nb = p.C / 16;
-  float amax_mu;
-  if (!p.hadamard) {
-    amax_mu = __uint_as_float(atomicAdd(&p.ctrl[kCtrlAmaxMu], 0u));
-  } else {
+  float amax_mu = s_amax_mu;
+  if (p.hadamard) {
     float a = 0.f;
-    for (int64_t b = threadIdx.x; b < nb; b += 256) {
+    for (int64_t b = tid; b < nb; b += 256) {
       float v[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) v[e] = __ldcg(p.mu + 16 * b + e);
@@ -275,8 +362,8 @@ __global__ void __launch_bounds__(256) colstats_finalize_kernel(FinalizeParams p
     amax_mu = block_max256(a, red);
   }
   const float s_g = tensor_scale_of(amax_mu);
-  if (threadIdx.x == 0) *p.mu_ts = s_g;
-  for (int64_t b = threadIdx.x; b < nb; b += 256) {
+  if (tid == 0) *p.mu_ts = s_g;
+  for (int64_t b = tid; b < nb; b += 256) {
     float v[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) v[e] = __ldcg(p.mu + 16 * b + e);
@@ -352,20 +439,26 @@ __global__ void __launch_bounds__(kQThreads, 2) split_quant_kernel(QuantParams p
   uint8_t* sstage_col = sstage_row + 1024;                // 1 KB: 2 scale chunks of the column layout
   __shared__ float red[8];
 
+  __shared__ int s_last;
+
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int ntiles = p.tiles_r * p.tiles_c;
   const bool split = p.mu != nullptr;
-  const float s_row = AMAX_ONLY ? 0.f : tensor_scale_of(__uint_as_float(p.ctrl[kCtrlAmaxRow]));
-  const float s_col = AMAX_ONLY ? 0.f : tensor_scale_of(__uint_as_float(p.ctrl[kCtrlAmaxCol]));
+
+  // the input was written before the previous kernel started: fetch the
+  // first tile while that kernel finishes
+  int buf = 0;
+  if ((int)blockIdx.x < ntiles) quant_issue_tile(p, qsm, blockIdx.x);
+  ptx::cp_async_commit();
+  pdl_wait_and_release();
+
+  const float s_row = AMAX_ONLY ? 0.f : __uint_as_float(__ldcg(&p.ctrl[kCtrlScaleRow]));
+  const float s_col = AMAX_ONLY ? 0.f : __uint_as_float(__ldcg(&p.ctrl[kCtrlScaleCol]));
   if (!AMAX_ONLY && blockIdx.x == 0 && threadIdx.x == 0) {
     if (p.row_ts) *p.row_ts = s_row;
     if (p.col_ts) *p.col_ts = s_col;
   }
   float amax_row = 0.f, amax_col = 0.f;
-
-  int buf = 0;
-  if ((int)blockIdx.x < ntiles) quant_issue_tile(p, qsm, blockIdx.x);
-  ptx::cp_async_commit();
   for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
     const int next = tile + gridDim.x;
     if (next < ntiles) quant_issue_tile(p, qsm + (buf ^ 1) * kQSmemTile, next);
@@ -517,11 +610,24 @@ __global__ void __launch_bounds__(kQThreads, 2) split_quant_kernel(QuantParams p
   }
   ptx::cp_async_wait<0>();
   if (AMAX_ONLY) {
+    // rotated maxima -> tensor scales; the last CTA converts and resets
     amax_row = block_max256(amax_row, red);
     amax_col = block_max256(amax_col, red);
     if (threadIdx.x == 0) {
       atomicMax(&p.ctrl[kCtrlAmaxRow], __float_as_uint(amax_row));
       atomicMax(&p.ctrl[kCtrlAmaxCol], __float_as_uint(amax_col));
+      __threadfence();
+      const unsigned t = atomicAdd(&p.ctrl[kCtrlAmaxTicket], 1u);
+      s_last = (t == gridDim.x - 1);
+    }
+    __syncthreads();
+    if (s_last && threadIdx.x == 0) {
+      __threadfence();
+      const float ar = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxRow], 0u));
+      const float ac = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxCol], 0u));
+      p.ctrl[kCtrlScaleRow] = __float_as_uint(tensor_scale_of(ar));
+      p.ctrl[kCtrlScaleCol] = __float_as_uint(tensor_scale_of(ac));
+      p.ctrl[kCtrlAmaxTicket] = 0u;
     }
   }
 }
@@ -538,6 +644,7 @@ __global__ void __launch_bounds__(256) rank1_gemv_kernel(const uint8_t* __restri
                                                          const float* __restrict__ w_ts, int64_t w_ld, int64_t N,
                                                          int64_t K, int64_t kc, float* __restrict__ out) {
   __shared__ float lut[16];
+  pdl_wait_and_release();
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_val(threadIdx.x);
   __syncthreads();
   const int lane = threadIdx.x & 31;
