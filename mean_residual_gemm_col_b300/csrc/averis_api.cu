@@ -87,16 +87,14 @@ averis_status set_attrs() {
   if (cudaFuncSetAttribute(split_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           GemmCfg<128>::SMEM) != cudaSuccess)
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM) !=
+      cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           GemmCfg<128>::SMEM) != cudaSuccess)
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM) !=
+      cudaSuccess)
     return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }
-
-averis_status launch_status() { return cudaGetLastError() == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA; }
 
 // ------------------------------------------------------------ geometry --
 
@@ -261,8 +259,8 @@ averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const floa
   averis_status st = device_info(&dev);
   if (st != AVERIS_OK) return st;
 
-  constexpr int BN = 128;
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg;
+  constexpr int BN = Cfg::BN;
   const int64_t ld = averis_nvfp4_ld(K);
   CUtensorMap ta, tb, td;
   if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->codes, (uint64_t)ld, (uint64_t)M, (uint64_t)ld, Cfg::BKB,
@@ -292,11 +290,9 @@ averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const floa
   p.err = dev->err_word;
   const int64_t ntiles = cdiv(M, Cfg::BM) * cdiv(N, BN);
   const int grid = (int)std::min<int64_t>(ntiles, dev->sms);
-  if (bf16)
-    gemm_nvfp4_kernel<BN, true><<<grid, 192, Cfg::SMEM, s>>>(ta, tb, td, p);
-  else
-    gemm_nvfp4_kernel<BN, false><<<grid, 192, Cfg::SMEM, s>>>(ta, tb, td, p);
-  return launch_status();
+  cudaError_t e = bf16 ? launch_pdl(gemm_nvfp4_kernel<true>, dim3(grid), dim3(192), Cfg::SMEM, s, ta, tb, td, p)
+                       : launch_pdl(gemm_nvfp4_kernel<false>, dim3(grid), dim3(192), Cfg::SMEM, s, ta, tb, td, p);
+  return e == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA;
 }
 
 averis_status rank1_impl(const averis_nvfp4* mu_q, const averis_nvfp4* w, float* out, cudaStream_t s) {

@@ -11,21 +11,26 @@
 // the mean term is broadcast, never materialised: paperlayer.ai summary,
 // section 3 Method).
 //
-// Design: persistent CTAs (one per SM), 128 x BN output tiles, K tiles of 256
-// elements (128 bytes of codes per row).  Warp roles:
+// Design: persistent CTAs (one per SM), 128 x 256 output tiles (M fastest,
+// so CTAs running together share B tiles in L2), K tiles of 256 elements
+// (128 bytes of codes per row), a 3-deep shared-memory ring.  Warp roles:
 //   warp 0     TMA producer: codes by 2-D tensor TMA (128-byte swizzle),
-//              block scales by 1-D bulk copies, into a STAGES-deep ring.
+//              block scales by 1-D bulk copies.
 //   warp 1     TMEM owner and MMA issuer: scale chunks SMEM->TMEM with
-//              tcgen05.cp, then tcgen05.mma kind::mxf4nvf4 (K = 64 per
-//              instruction) accumulating in TMEM; tcgen05.commit frees the
-//              SMEM stage and, after the last K tile, hands the accumulator
-//              to the epilogue.
+//              tcgen05.cp, then tcgen05.mma kind::mxf4nvf4 128x256x64
+//              accumulating in TMEM; tcgen05.commit frees the stage and,
+//              after the last K tile, hands the accumulator to the epilogue.
 //   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, alpha scaling and
-//              the rank-one terms in binary32, SMEM staging (128-byte
-//              swizzle) and TMA tensor stores (which clip ragged edges).
-// Two accumulator buffers (BN = 128) let the epilogue of tile t overlap the
-// main loop of tile t+1.  Every wait is bounded; on timeout the kernel sets
-// the error word, drains its own tensor-core work and frees its TMEM.
+//              the rank-one terms in binary32 (vector entries fetched once
+//              per 32 columns and broadcast by warp shuffles), SMEM staging
+//              (128-byte swizzle), TMA tensor stores (which clip ragged edges).
+// One 256-column accumulator leaves TMEM room for the scale stages.  With a
+// bf16 output the epilogue moves the whole accumulator into registers
+// (packed bf16) and releases TMEM before storing, so the next tile's MMAs
+// overlap the stores.  Every wait is bounded; on timeout the kernel sets the
+// error word, drains its own tensor-core work and frees its TMEM.  Launched
+// with programmatic dependent launch: set-up runs before the wait for the
+// previous kernel.
 #pragma once
 
 #include <cstdint>
@@ -55,12 +60,11 @@ enum : int { kErrNone = 0, kErrProducer = 1, kErrMma = 2, kErrEpilogue = 3, kErr
 
 constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clock
 
-template <int BN>
 struct GemmCfg {
   static constexpr int BM = 128;
+  static constexpr int BN = 256;
   static constexpr int BKB = 128;  // bytes of codes per row per K tile (256 elements)
-  static constexpr int STAGES = BN == 128 ? 4 : 3;
-  static constexpr int ACC_BUFS = BN == 128 ? 2 : 1;
+  static constexpr int STAGES = 3;
   static constexpr int A_BYTES = BM * BKB;
   static constexpr int B_BYTES = BN * BKB;
   static constexpr int SFA_BYTES = 4 * 512;
@@ -74,31 +78,46 @@ struct GemmCfg {
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
   static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
-  // TMEM columns: accumulators, then per stage 16 SFA columns + BN/8 SFB columns
-  static constexpr int SF_BASE = ACC_BUFS * BN;
+  // TMEM columns: the accumulator, then per stage 16 SFA columns + BN/8 SFB columns
+  static constexpr int SF_BASE = BN;
   static constexpr int SFB_COLS_PER_STEP = BN / 32;
   static constexpr int SF_STAGE_COLS = 16 + 4 * SFB_COLS_PER_STEP;
   static constexpr int TMEM_COLS = 512;
   static_assert(OFF_EPI % 1024 == 0, "epilogue staging must be 1024-byte aligned");
   static_assert(SF_BASE + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM overflow");
+  static_assert(SMEM <= 227 * 1024, "shared memory overflow");
   // instruction descriptor: E2M1 x E2M1 (format 1), K-major A and B, UE4M3 scales,
   // N >> 3 at bit 17, M >> 4 at bit 24
   static constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 };
 
-template <int BN, bool BF16_OUT>
+// Epilogue value of one accumulator column chunk: alpha * acc + col_add + rterm * col_vec.
+// `cadd`/`cvec` hold the vector entry of column (chunk + lane) in each lane.
+__device__ __forceinline__ void epi_math(float (&f)[32], const uint32_t (&v)[32], float alpha, bool has_add,
+                                         float cadd, bool has_outer, float rterm, float cvec) {
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    float x = alpha * __uint_as_float(v[j]);
+    if (has_add) x += __shfl_sync(0xffffffffu, cadd, j);
+    if (has_outer) x = fmaf(rterm, __shfl_sync(0xffffffffu, cvec, j), x);
+    f[j] = x;
+  }
+}
+
+template <bool BF16_OUT>
 __global__ void __launch_bounds__(192, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
-  using Cfg = GemmCfg<BN>;
+  using Cfg = GemmCfg;
   constexpr int STAGES = Cfg::STAGES;
+  constexpr int BN = Cfg::BN;
   extern __shared__ uint8_t gsm_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
-  uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
+  uint64_t* tempty = tfull + 1;
+  uint64_t* drain = tempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -107,10 +126,8 @@ __global__ void __launch_bounds__(192, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
     }
-    for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(&tfull[a], 1);
-      ptx::mbar_init(&tempty[a], 4);
-    }
+    ptx::mbar_init(tfull, 1);
+    ptx::mbar_init(tempty, 4);
     ptx::mbar_init(drain, 1);
     ptx::fence_mbar_init();
   }
@@ -127,6 +144,8 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // operands, scales and epilogue vectors may come from the previous kernel
+  ptx::pdl_wait_and_release();
 
   const int num_m = (p.M + Cfg::BM - 1) / Cfg::BM;
   const int num_n = (p.N + BN - 1) / BN;
@@ -139,15 +158,15 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int mt = tile % num_m, nt = tile / num_m;
+        int nsfb = 0;
+#pragma unroll
+        for (int h = 0; h < BN / 128; ++h) nsfb += (nt * (BN / 128) + h) < p.rb_b ? 1 : 0;
         for (int kt = 0; kt < nkt; ++kt) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, kWaitLimit)) {
             atomicExch(p.err, kErrProducer);
             goto done;
           }
           const int ns = min(4, p.kc - 4 * kt);
-          int nsfb = 0;
-#pragma unroll
-          for (int h = 0; h < BN / 128; ++h) nsfb += (nt * (BN / 128) + h) < p.rb_b ? 1 : 0;
           const uint32_t bytes = Cfg::A_BYTES + Cfg::B_BYTES + (uint32_t)ns * 512u * (1u + (uint32_t)nsfb);
           ptx::mbar_arrive_expect_tx(&full[stage], bytes);
           ptx::tma_load_2d(smem + Cfg::OFF_A + stage * Cfg::A_BYTES, &tmA, kt * Cfg::BKB, mt * Cfg::BM, &full[stage]);
@@ -175,14 +194,11 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;
       bool issued = false;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-        const int acc = Cfg::ACC_BUFS == 2 ? (it & 1) : 0;
-        const uint32_t acc_phase = Cfg::ACC_BUFS == 2 ? ((it >> 1) & 1) : (it & 1);
-        if (!ptx::mbar_wait(&tempty[acc], acc_phase ^ 1u, kWaitLimit)) {
+        if (!ptx::mbar_wait(tempty, (it & 1) ^ 1u, kWaitLimit)) {
           atomicExch(p.err, kErrMma);
           break;
         }
         ptx::tc_fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
         bool ok = true;
         for (int kt = 0; kt < nkt; ++kt) {
           if (!ptx::mbar_wait(&full[stage], phase, kWaitLimit)) {
@@ -208,7 +224,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int g = 0; g < ns; ++g) {
             const uint64_t adesc = ptx::smem_desc(a_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
             const uint64_t bdesc = ptx::smem_desc(b_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
-            ptx::tc_mma_nvf4(d_tmem, adesc, bdesc, Cfg::IDESC, sfa_t + 4u * g,
+            ptx::tc_mma_nvf4(tmem, adesc, bdesc, Cfg::IDESC, sfa_t + 4u * g,
                              sfb_t + (uint32_t)(Cfg::SFB_COLS_PER_STEP * g), (kt | g) != 0 ? 1u : 0u);
           }
           issued = true;
@@ -219,7 +235,7 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
         if (!ok) break;
-        ptx::tc_commit(&tfull[acc]);
+        ptx::tc_commit(tfull);
       }
       if (issued) {
         // drain: every MMA and copy this thread issued has completed
@@ -231,75 +247,99 @@ __global__ void __launch_bounds__(192, 1)
     // epilogue warps: TMEM lane quarter (warp % 4) holds tile rows 32*(warp%4) .. +31
     const int q = warp & 3;
     const float alpha = __ldg(p.ts_a) * __ldg(p.ts_b);
+    const bool has_add = p.col_add != nullptr;
+    const bool has_outer = p.row_vec != nullptr;
     uint8_t* stage_base = smem + Cfg::OFF_EPI + q * 2 * Cfg::EPI_BUF;
     int sbuf = 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
       const int mt = tile % num_m, nt = tile / num_m;
-      const int acc = Cfg::ACC_BUFS == 2 ? (it & 1) : 0;
-      const uint32_t acc_phase = Cfg::ACC_BUFS == 2 ? ((it >> 1) & 1) : (it & 1);
-      if (!ptx::mbar_wait(&tfull[acc], acc_phase, kWaitLimit)) {
+      const int row = mt * Cfg::BM + q * 32 + lane;
+      const int row0 = mt * Cfg::BM + q * 32;
+      const float rterm = (has_outer && row < p.M) ? p.outer * __ldg(p.row_vec + row) : 0.f;
+      if (!ptx::mbar_wait(tfull, it & 1, kWaitLimit)) {
         atomicExch(p.err, kErrEpilogue);
         break;
       }
       ptx::tc_fence_after();
-      const int row = mt * Cfg::BM + q * 32 + lane;
-      const float rterm = (p.row_vec != nullptr && row < p.M) ? p.outer * __ldg(p.row_vec + row) : 0.f;
-      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
-      constexpr int COLS_PER_STORE = BF16_OUT ? 64 : 32;
-#pragma unroll 1
-      for (int c = 0; c < BN; c += COLS_PER_STORE) {
-        float f[COLS_PER_STORE];
-#pragma unroll
-        for (int h = 0; h < COLS_PER_STORE / 32; ++h) {
-          uint32_t v[32];
-          ptx::tmem_ld32(t_row + (uint32_t)(c + 32 * h), v);
-          ptx::tmem_ld_wait();
-#pragma unroll
-          for (int j = 0; j < 32; ++j) f[32 * h + j] = alpha * __uint_as_float(v[j]);
-        }
-        const int col0 = nt * BN + c;
-        if (p.col_add != nullptr || p.row_vec != nullptr) {
-#pragma unroll
-          for (int j = 0; j < COLS_PER_STORE; ++j) {
-            const int col = col0 + j;
-            if (col < p.N) {
-              if (p.col_add != nullptr) f[j] += __ldg(p.col_add + col);
-              if (p.row_vec != nullptr) f[j] = fmaf(rterm, __ldg(p.col_vec + col), f[j]);
-            }
-          }
-        }
+      const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
+
+      // vector entries of the 32 columns starting at c, one per lane
+      auto vec_at = [&](const float* v, int c) -> float {
+        const int col = nt * BN + c + lane;
+        return (v != nullptr && col < p.N) ? __ldg(v + col) : 0.f;
+      };
+      // stage one 32-row x 128-byte box in swizzled SMEM and store it with TMA
+      auto store_box = [&](const uint4 (&w)[8], int col0) {
         uint8_t* sb = stage_base + sbuf * Cfg::EPI_BUF;
         if (lane == 0) ptx::bulk_wait_read<1>();
         __syncwarp();
         uint8_t* srow = sb + lane * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          uint4 w;
-          if (BF16_OUT) {
-            __nv_bfloat162 b0 = __floats2bfloat162_rn(f[8 * k + 0], f[8 * k + 1]);
-            __nv_bfloat162 b1 = __floats2bfloat162_rn(f[8 * k + 2], f[8 * k + 3]);
-            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[8 * k + 4], f[8 * k + 5]);
-            __nv_bfloat162 b3 = __floats2bfloat162_rn(f[8 * k + 6], f[8 * k + 7]);
-            w = make_uint4(*reinterpret_cast<uint32_t*>(&b0), *reinterpret_cast<uint32_t*>(&b1),
-                           *reinterpret_cast<uint32_t*>(&b2), *reinterpret_cast<uint32_t*>(&b3));
-          } else {
-            w = make_uint4(__float_as_uint(f[4 * k]), __float_as_uint(f[4 * k + 1]), __float_as_uint(f[4 * k + 2]),
-                           __float_as_uint(f[4 * k + 3]));
-          }
-          *reinterpret_cast<uint4*>(srow + ((k ^ (lane & 7)) * 16)) = w;
-        }
+        for (int k = 0; k < 8; ++k) *reinterpret_cast<uint4*>(srow + ((k ^ (lane & 7)) * 16)) = w[k];
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::tma_store_2d(&tmD, sb, col0, mt * Cfg::BM + q * 32);
+          ptx::tma_store_2d(&tmD, sb, col0, row0);
           ptx::bulk_commit();
         }
         sbuf ^= 1;
+      };
+
+      if (BF16_OUT) {
+        // whole accumulator -> packed bf16 registers, release TMEM, then store
+        uint32_t packed[BN / 2];
+#pragma unroll
+        for (int c = 0; c < BN; c += 32) {
+          const float cadd = vec_at(p.col_add, c);
+          const float cvec = vec_at(p.col_vec, c);
+          uint32_t v[32];
+          ptx::tmem_ld32(t_row + (uint32_t)c, v);
+          ptx::tmem_ld_wait();
+          float f[32];
+          epi_math(f, v, alpha, has_add, cadd, has_outer, rterm, cvec);
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
+            packed[c / 2 + j] = *reinterpret_cast<uint32_t*>(&b2);
+          }
+        }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(tempty);
+#pragma unroll
+        for (int c = 0; c < BN; c += 64) {
+          uint4 w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            w[k] = make_uint4(packed[c / 2 + 4 * k], packed[c / 2 + 4 * k + 1], packed[c / 2 + 4 * k + 2],
+                              packed[c / 2 + 4 * k + 3]);
+          store_box(w, nt * BN + c);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN; c += 32) {
+          const float cadd = vec_at(p.col_add, c);
+          const float cvec = vec_at(p.col_vec, c);
+          uint32_t v[32];
+          ptx::tmem_ld32(t_row + (uint32_t)c, v);
+          ptx::tmem_ld_wait();
+          if (c + 32 == BN) {
+            // last chunk is in registers: the accumulator may be overwritten
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(tempty);
+          }
+          float f[32];
+          epi_math(f, v, alpha, has_add, cadd, has_outer, rterm, cvec);
+          uint4 w[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            w[k] = make_uint4(__float_as_uint(f[4 * k]), __float_as_uint(f[4 * k + 1]), __float_as_uint(f[4 * k + 2]),
+                              __float_as_uint(f[4 * k + 3]));
+          store_box(w, nt * BN + c);
+        }
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&tempty[acc]);
     }
     if (lane == 0) ptx::bulk_wait<0>();
     __syncwarp();

@@ -99,6 +99,17 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+// ------------------------------------------------- dependent launch --
+
+// Programmatic dependent launch: wait until the previous kernel of the stream
+// has completed and its writes are visible, then let the next kernel start
+// launching (its own wait keeps it from reading what this one writes).  A
+// no-op for kernels launched without the programmatic-serialization attribute.
+__device__ __forceinline__ void pdl_wait_and_release() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------ cp.async --
 
 // 16-byte global->shared copy; src_bytes < 16 zero-fills the rest (0 reads nothing).

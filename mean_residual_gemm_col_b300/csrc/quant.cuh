@@ -58,13 +58,6 @@ __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t k, int64_t kc
   return ((r >> 7) * kc + (k >> 2)) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5) + (k & 3);
 }
 
-// Programmatic dependent launch: wait until the previous kernel of the stream
-// has completed and its writes are visible, then let the next kernel start
-// launching (its own wait keeps it from reading what this one writes).
-__device__ __forceinline__ void pdl_wait_and_release() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
 
 // Block-wide max of non-negative floats (blockDim 256).
 __device__ __forceinline__ float block_max256(float v, float* red) {
@@ -176,7 +169,7 @@ __global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
   __shared__ float s_mx[8][64], s_mn[8][64];
   __shared__ float red[8];
   __shared__ int s_last;
-  pdl_wait_and_release();
+  ptx::pdl_wait_and_release();
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = tid & 7;     // 8-column group inside the strip
@@ -450,7 +443,7 @@ __global__ void __launch_bounds__(kQThreads, 2) split_quant_kernel(QuantParams p
   int buf = 0;
   if ((int)blockIdx.x < ntiles) quant_issue_tile(p, qsm, blockIdx.x);
   ptx::cp_async_commit();
-  pdl_wait_and_release();
+  ptx::pdl_wait_and_release();
 
   const float s_row = AMAX_ONLY ? 0.f : __uint_as_float(__ldcg(&p.ctrl[kCtrlScaleRow]));
   const float s_col = AMAX_ONLY ? 0.f : __uint_as_float(__ldcg(&p.ctrl[kCtrlScaleCol]));
@@ -644,7 +637,7 @@ __global__ void __launch_bounds__(256) rank1_gemv_kernel(const uint8_t* __restri
                                                          const float* __restrict__ w_ts, int64_t w_ld, int64_t N,
                                                          int64_t K, int64_t kc, float* __restrict__ out) {
   __shared__ float lut[16];
-  pdl_wait_and_release();
+  ptx::pdl_wait_and_release();
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_val(threadIdx.x);
   __syncthreads();
   const int lane = threadIdx.x & 31;
