@@ -18,7 +18,7 @@ namespace {
 using namespace averis;
 
 constexpr int kMaxDevices = 64;
-constexpr int kStatsTargetCtas = 592;  // CTA count target of the stats pass (4 per SM of a B300)
+constexpr int kStatsTargetCtas = 296;  // CTA count target of the stats pass (one wave at 2 per SM of a B300)
 
 __device__ int g_device_error = 0;
 
@@ -110,9 +110,9 @@ StatsGeom stats_geom(int64_t R, int64_t C) {
   g.nstrips = (int)cdiv(C, 64);
   g.gx = std::min(g.nstrips, (int)kMaxStripGroups);
   int64_t nrb = cdiv(kStatsTargetCtas, g.gx);
-  nrb = std::max<int64_t>(1, std::min<int64_t>(nrb, cdiv(R, 128)));
+  nrb = std::max<int64_t>(1, std::min<int64_t>(nrb, cdiv(R, 512)));  // at least 2 load groups per thread
   int64_t rp = cdiv(R, nrb);
-  rp = cdiv(rp, 128) * 128;
+  rp = cdiv(rp, 256) * 256;
   g.rows_per = rp;
   g.nrb = (int)cdiv(R, rp);
   return g;
@@ -171,6 +171,7 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   averis_status st = device_info(&dev);
   if (st != AVERIS_OK) return st;
 
+  if (out_row == nullptr && out_col == nullptr && !split) return AVERIS_OK;  // nothing to compute
   uint8_t* w = static_cast<uint8_t*>(ws);
   unsigned* ctrl = reinterpret_cast<unsigned*>(w);
   ColPartial* part = reinterpret_cast<ColPartial*>(w + kCtrlBytes);
@@ -188,22 +189,23 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   sp.split = split ? 1 : 0;
   sp.hadamard = had ? 1 : 0;
   sp.mu = mu;
-  if (split) {
-    sp.mu_codes = mu_q->codes;
-    sp.mu_scales = mu_q->scales;
-    sp.mu_ts = mu_q->tensor_scale;
-    sp.mu_hat = mu_hat;
-  }
-  sp.kc = cdiv(C, 64);
   if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), 0, s, sp) != cudaSuccess) return AVERIS_ERR_CUDA;
 
-  if (out_row == nullptr && out_col == nullptr) return AVERIS_OK;
+  // The quantize pass also writes the NVFP4 mean (one of its CTAs) and resets
+  // the control block, so it runs even with no residual layout requested.
   QuantParams qp{};
-  qp.x = xb;
   qp.R = R;
   qp.C = C;
   qp.mu = split ? mu : nullptr;
+  if (split) {
+    qp.mu_codes = mu_q->codes;
+    qp.mu_scales = mu_q->scales;
+    qp.mu_ts = mu_q->tensor_scale;
+    qp.mu_hat = mu_hat;
+    qp.mu_kc = cdiv(C, 64);
+  }
   qp.ctrl = ctrl;
+  qp.err = dev->err_word;
   qp.hadamard = had ? 1 : 0;
   if (out_row != nullptr) {
     qp.row_codes = out_row->codes;
@@ -221,11 +223,23 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   }
   qp.tiles_r = (int)cdiv(R, kQTile);
   qp.tiles_c = (int)cdiv(C, kQTile);
+  CUtensorMap tx;
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)C, (cuuint64_t)R};
+    const cuuint64_t strides[1] = {(cuuint64_t)C * 2};
+    const cuuint32_t box[2] = {64, kQTile};
+    const cuuint32_t estr[2] = {1, 1};
+    if (g_encode(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(x), dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return AVERIS_ERR_CUDA;
+  }
+  if (out_row == nullptr && out_col == nullptr) qp.tiles_r = 0;  // mean only
   const int ntiles = qp.tiles_r * qp.tiles_c;
-  const int grid = (int)std::min<int64_t>(ntiles, 2 * (int64_t)dev->sms);
-  if (had && launch_pdl(split_quant_kernel<true>, dim3(grid), dim3(kQThreads), kQSmem, s, qp) != cudaSuccess)
+  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, 2 * (int64_t)dev->sms));
+  if (had && launch_pdl(split_quant_kernel<true>, dim3(grid), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (launch_pdl(split_quant_kernel<false>, dim3(grid), dim3(kQThreads), kQSmem, s, qp) != cudaSuccess)
+  if (launch_pdl(split_quant_kernel<false>, dim3(grid), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }

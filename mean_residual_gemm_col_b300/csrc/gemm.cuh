@@ -56,9 +56,6 @@ struct GemmParams {
   int* err;
 };
 
-enum : int { kErrNone = 0, kErrProducer = 1, kErrMma = 2, kErrEpilogue = 3, kErrDrain = 4 };
-
-constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clock
 
 struct GemmCfg {
   static constexpr int BM = 128;

@@ -208,6 +208,19 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
 
 }  // namespace ptx
 
+// Codes a kernel writes to the library's device error word when a bounded
+// wait gives up (read back by averis_last_device_error).
+enum : int {
+  kErrNone = 0,
+  kErrProducer = 1,   // GEMM TMA producer: a stage was never released
+  kErrMma = 2,        // GEMM MMA issuer: operands or accumulator never arrived
+  kErrEpilogue = 3,   // GEMM epilogue: accumulator never completed
+  kErrDrain = 4,      // GEMM: own tensor-core work did not complete
+  kErrQuantLoad = 5   // quantize pass: an input tile never arrived
+};
+
+constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clock
+
 // Exact binary32 value of a non-negative E4M3 code (0x7F is never produced).
 __device__ __forceinline__ float e4m3_value(uint32_t code) {
   const uint32_t e = (code >> 3) & 15u, m = code & 7u;

@@ -28,18 +28,16 @@
 
 namespace averis {
 
-// Control block at the head of every quantize workspace.  Every word below
-// kCtrlScaleRow is zero at rest: the kernel that counts on a ticket or
-// accumulates a maximum resets it before it finishes, so a workspace that
-// starts zeroed stays usable for any later call without a memset.
+// Control block at the head of every quantize workspace.  Every word is zero
+// at rest: the stats pass accumulates maxima with atomicMax and resets its
+// strip tickets itself; the last CTA of the quantize pass (ticket) resets the
+// maxima after every reader is done, so a workspace that starts zeroed stays
+// usable for any later call without a memset.
 enum : int {
-  kCtrlTicket = 0,       // stats pass: strips finished
-  kCtrlAmaxRow = 1,      // residual max magnitude, layout blocked along columns (float bits)
-  kCtrlAmaxCol = 2,      // same, layout blocked along rows
-  kCtrlAmaxMu = 3,       // max |mu|
-  kCtrlAmaxTicket = 4,   // rotated-amax pass: CTAs finished
-  kCtrlScaleRow = 8,     // tensor scales handed to the quantize pass (written every call)
-  kCtrlScaleCol = 9,
+  kCtrlAmaxRes = 1,      // residual max magnitude (float bits), both layouts
+  kCtrlAmaxRowH = 5,     // rotated residual max, layout blocked along columns (Hadamard)
+  kCtrlAmaxColH = 6,     // rotated residual max, layout blocked along rows (Hadamard)
+  kCtrlQuantTicket = 7,  // quantize pass: CTAs finished
   kCtrlStrip = 64,       // per-strip-group tickets of the stats pass
   kMaxStripGroups = 1024,
   kCtrlWords = kCtrlStrip + kMaxStripGroups
@@ -58,6 +56,66 @@ __device__ __forceinline__ int64_t scale_offset(int64_t r, int64_t k, int64_t kc
   return ((r >> 7) * kc + (k >> 2)) * 512 + 16 * (r & 31) + 4 * ((r & 127) >> 5) + (k & 3);
 }
 
+
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  return (uint64_t)__float_as_uint(a) | ((uint64_t)__float_as_uint(b) << 32);
+}
+__device__ __forceinline__ float f2lo(uint64_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2hi(uint64_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
+// Two binary32 subtractions / multiplications, each rounded to nearest even (packed issue).
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// The two bf16 values of a packed word as a binary32 pair (exact).
+__device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return f2pack(bf16lo(w), bf16hi(w)); }
+// Element-wise max / min of two packed bf16 pairs (exact).
+__device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+__device__ __forceinline__ uint32_t bmin2(uint32_t a, uint32_t b) {
+  __nv_bfloat162 r = __hmin2(*reinterpret_cast<__nv_bfloat162*>(&a), *reinterpret_cast<__nv_bfloat162*>(&b));
+  return *reinterpret_cast<uint32_t*>(&r);
+}
+
+// Unevaluated sum hi + lo of two binary32 values (|lo| <= ulp(hi) / 2): the
+// column sums are combined in this form, exactly enough for the mean and
+// without float64 arithmetic (slow on this part).
+struct F2 {
+  float hi, lo;
+};
+__device__ __forceinline__ F2 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return {s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb))};
+}
+__device__ __forceinline__ F2 fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return {s, __fsub_rn(b, __fsub_rn(s, a))};
+}
+__device__ __forceinline__ F2 df_add(F2 a, F2 b) {
+  const F2 s = two_sum(a.hi, b.hi);
+  return fast_two_sum(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+// binary32 of (hi + lo) / n for an integer count n < 2^24 (exact in binary32).
+__device__ __forceinline__ float df_div_count(F2 a, float n) {
+  const float q = __fdiv_rn(a.hi, n);
+  const float r = __fadd_rn(__fmaf_rn(-q, n, a.hi), a.lo);  // a - q n, the product residual is exact
+  return __fadd_rn(q, __fdiv_rn(r, n));
+}
 
 // Block-wide max of non-negative floats (blockDim 256).
 __device__ __forceinline__ float block_max256(float v, float* red) {
@@ -136,19 +194,13 @@ __device__ __forceinline__ float e2m1_val(uint32_t c4) {
 struct StatsParams {
   const __nv_bfloat16* x;
   int64_t R, C;
-  int64_t rows_per;   // rows per CTA row block (multiple of 128)
+  int64_t rows_per;   // rows per CTA row block (multiple of 256)
   int nstrips;        // ceil(C / 64) column strips of 64
   ColPartial* part;   // [gridDim.y][C] per-row-block partials
   unsigned* ctrl;
   int split;          // mean split on
   int hadamard;       // rotation on (the rotated residual's maximum comes from the amax pass)
   float* mu;          // [C] out (split)
-  // quantized mean (split): [1, C]
-  uint8_t* mu_codes;
-  uint8_t* mu_scales;
-  float* mu_ts;
-  float* mu_hat;      // [C] dequantized, unrotated
-  int64_t kc;         // ceil(C / 64)
 };
 
 // Column statistics in one pass over X, with the combine fused in.
@@ -156,16 +208,16 @@ struct StatsParams {
 // grid (strip groups, row blocks), 256 threads.  CTA (g, b) reads rows
 // [b*rows_per, (b+1)*rows_per) of the 64-column strips g, g+gridDim.x, ...:
 // thread t owns 8 adjacent columns (16-byte loads) of rows t/8, t/8+32, ...,
-// keeps a Kahan-compensated binary32 sum plus max and min per column, and the
-// 32 row lanes are combined in float64 in a fixed order.  The last CTA of a
-// strip group to finish (ticket) combines the row-block partials of its
-// strips in row-block order -- the result does not depend on which CTA is
-// last -- giving mu_j = fl32(S_j / R) and the residual's exact maximum
-// magnitude max(|fl32(max_j - mu_j)|, |fl32(min_j - mu_j)|) (binary32
-// subtraction is monotone).  The last strip group overall turns the maxima
-// into the two tensor scales and quantizes mu as a [1, C] NVFP4 row.
-__global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
-  __shared__ double s_sum[8][64];
+// keeps a Kahan-compensated binary32 sum plus max and min per column (packed
+// bf16 max / min, pairs of columns summed with packed binary32 adds), and the
+// 32 row lanes are combined as hi + lo binary32 pairs in a fixed order.  The
+// last CTA of a strip group to finish (ticket) combines the row-block
+// partials of its strips in row-block order -- the result does not depend on
+// which CTA is last -- giving mu_j = fl32(S_j / R) and the residual's exact
+// maximum magnitude max(|fl32(max_j - mu_j)|, |fl32(min_j - mu_j)|) (binary32
+// subtraction is monotone), folded into the control block with atomicMax.
+__global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
+  __shared__ F2 s_sum[8][64];
   __shared__ float s_mx[8][64], s_mn[8][64];
   __shared__ float red[8];
   __shared__ int s_last;
@@ -179,81 +231,103 @@ __global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
 
   for (int strip = blockIdx.x; strip < p.nstrips; strip += gridDim.x) {
     const int64_t c0 = (int64_t)strip * 64 + 8 * g8;
-    float s[8], c[8], mx[8], mn[8];
+    // column pairs (2w, 2w+1): Kahan-compensated binary32 sums, packed bf16 max / min
+    uint64_t s2[4], c2[4];
+    uint32_t mx2[4], mn2[4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      s[e] = 0.f;
-      c[e] = 0.f;
-      mx[e] = -FLT_MAX;
-      mn[e] = FLT_MAX;
+    for (int w = 0; w < 4; ++w) {
+      s2[w] = 0ull;
+      c2[w] = 0ull;
+      mx2[w] = 0xFF80FF80u;  // -inf, -inf
+      mn2[w] = 0x7F807F80u;  // +inf, +inf
     }
+    auto kahan = [&](int w, uint64_t t) {
+      const uint64_t y = sub2(t, c2[w]);
+      const uint64_t tt = add2(s2[w], y);
+      c2[w] = sub2(sub2(tt, s2[w]), y);
+      s2[w] = tt;
+    };
+    // 8 rows (stride 32) at a time: pairwise sums, then one compensated add
+    auto group = [&](const uint4 (&v)[8]) {
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t x[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) x[j] = w == 0 ? v[j].x : w == 1 ? v[j].y : w == 2 ? v[j].z : v[j].w;
+        mx2[w] = bmax2(mx2[w], bmax2(bmax2(bmax2(x[0], x[1]), bmax2(x[2], x[3])), bmax2(bmax2(x[4], x[5]), bmax2(x[6], x[7]))));
+        mn2[w] = bmin2(mn2[w], bmin2(bmin2(bmin2(x[0], x[1]), bmin2(x[2], x[3])), bmin2(bmin2(x[4], x[5]), bmin2(x[6], x[7]))));
+        const uint64_t t = add2(add2(add2(bf2_to_f2(x[0]), bf2_to_f2(x[1])), add2(bf2_to_f2(x[2]), bf2_to_f2(x[3]))),
+                                add2(add2(bf2_to_f2(x[4]), bf2_to_f2(x[5])), add2(bf2_to_f2(x[6]), bf2_to_f2(x[7]))));
+        kahan(w, t);
+      }
+    };
     if (c0 < p.C) {
-      const __nv_bfloat16* base = p.x + c0;
-      for (int64_t r = rb0 + rl; r < rb1; r += 128) {
-        uint4 v[4];
-        bool ok[4];
+      const __nv_bfloat16* base = p.x + c0 + (rb0 + rl) * p.C;
+      const int64_t nrow = rb1 > rb0 + rl ? (rb1 - rb0 - rl + 31) / 32 : 0;  // this thread's rows
+      const int64_t ng = nrow / 8;
+      const int64_t step = 32 * p.C;
+      auto load = [&](uint4 (&v)[8], int64_t g) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int64_t rr = r + 32 * j;
-          ok[j] = rr < rb1;
-          v[j] = ok[j] ? __ldg(reinterpret_cast<const uint4*>(base + rr * p.C)) : make_uint4(0, 0, 0, 0);
-        }
+        for (int j = 0; j < 8; ++j) v[j] = __ldg(reinterpret_cast<const uint4*>(base + (8 * g + j) * step));
+      };
+      // two register buffers: the next group's loads are in flight while one is summed
+      uint4 va[8], vb[8];
+      if (ng > 0) load(va, 0);
+      for (int64_t g = 0; g < ng; g += 2) {
+        if (g + 1 < ng) load(vb, g + 1);
+        group(va);
+        if (g + 1 >= ng) break;
+        if (g + 2 < ng) load(va, g + 2);
+        group(vb);
+      }
+      for (int64_t i = 8 * ng; i < nrow; ++i) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + i * step));
+        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float a[4];
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint32_t w = (e >> 1) == 0 ? v[j].x : (e >> 1) == 1 ? v[j].y : (e >> 1) == 2 ? v[j].z : v[j].w;
-            a[j] = (e & 1) ? bf16hi(w) : bf16lo(w);
-            if (ok[j]) {
-              mx[e] = fmaxf(mx[e], a[j]);
-              mn[e] = fminf(mn[e], a[j]);
-            }
-          }
-          // rows that are out of range contribute an exact 0 to the sum
-          const float t = __fadd_rn(__fadd_rn(a[0], a[1]), __fadd_rn(a[2], a[3]));
-          const float y = __fsub_rn(t, c[e]);
-          const float tt = __fadd_rn(s[e], y);
-          c[e] = __fsub_rn(__fsub_rn(tt, s[e]), y);
-          s[e] = tt;
+        for (int w = 0; w < 4; ++w) {
+          mx2[w] = bmax2(mx2[w], x[w]);
+          mn2[w] = bmin2(mn2[w], x[w]);
+          kahan(w, bf2_to_f2(x[w]));
         }
       }
     }
     // combine the 4 row lanes of this warp that share the columns (lanes differ by 8, 16)
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-      double d = (double)s[e] - (double)c[e];
-      d += __shfl_xor_sync(0xffffffffu, d, 8);
-      d += __shfl_xor_sync(0xffffffffu, d, 16);
-      float m1 = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
-      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 16));
-      float m2 = fminf(mn[e], __shfl_xor_sync(0xffffffffu, mn[e], 8));
-      m2 = fminf(m2, __shfl_xor_sync(0xffffffffu, m2, 16));
-      if (lane < 8) {
-        s_sum[warp][8 * lane + e] = d;
-        s_mx[warp][8 * lane + e] = m1;
-        s_mn[warp][8 * lane + e] = m2;
+    for (int w = 0; w < 4; ++w) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int e = 2 * w + h;
+        const float sv = h ? f2hi(s2[w]) : f2lo(s2[w]), cv = h ? f2hi(c2[w]) : f2lo(c2[w]);
+        F2 d = fast_two_sum(sv, -cv);
+        F2 o{__shfl_xor_sync(0xffffffffu, d.hi, 8), __shfl_xor_sync(0xffffffffu, d.lo, 8)};
+        d = (lane & 8) ? df_add(o, d) : df_add(d, o);
+        o = F2{__shfl_xor_sync(0xffffffffu, d.hi, 16), __shfl_xor_sync(0xffffffffu, d.lo, 16)};
+        d = (lane & 16) ? df_add(o, d) : df_add(d, o);
+        const float mxv = h ? bf16hi(mx2[w]) : bf16lo(mx2[w]), mnv = h ? bf16hi(mn2[w]) : bf16lo(mn2[w]);
+        float m1 = fmaxf(mxv, __shfl_xor_sync(0xffffffffu, mxv, 8));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, 16));
+        float m2 = fminf(mnv, __shfl_xor_sync(0xffffffffu, mnv, 8));
+        m2 = fminf(m2, __shfl_xor_sync(0xffffffffu, m2, 16));
+        if (lane < 8) {
+          s_sum[warp][8 * lane + e] = d;
+          s_mx[warp][8 * lane + e] = m1;
+          s_mn[warp][8 * lane + e] = m2;
+        }
       }
     }
     __syncthreads();
     if (tid < 64) {
       const int64_t col = (int64_t)strip * 64 + tid;
-      double acc = 0.0;
-      float m1 = -FLT_MAX, m2 = FLT_MAX;
+      F2 acc = s_sum[0][tid];
+      float m1 = s_mx[0][tid], m2 = s_mn[0][tid];
 #pragma unroll
-      for (int w = 0; w < 8; ++w) {
-        acc += s_sum[w][tid];
+      for (int w = 1; w < 8; ++w) {
+        acc = df_add(acc, s_sum[w][tid]);
         m1 = fmaxf(m1, s_mx[w][tid]);
         m2 = fminf(m2, s_mn[w][tid]);
       }
-      if (col < p.C) {
-        ColPartial q;
-        q.s_hi = (float)acc;
-        q.s_lo = (float)(acc - (double)q.s_hi);
-        q.mx = m1;
-        q.mn = m2;
-        *reinterpret_cast<float4*>(p.part + (int64_t)blockIdx.y * p.C + col) = make_float4(q.s_hi, q.s_lo, q.mx, q.mn);
-      }
+      if (col < p.C)
+        *reinterpret_cast<float4*>(p.part + (int64_t)blockIdx.y * p.C + col) = make_float4(acc.hi, acc.lo, m1, m2);
     }
     __syncthreads();
   }
@@ -269,19 +343,27 @@ __global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
   if (!s_last) return;
   __threadfence();
 
-  float a_res = 0.f, a_mu = 0.f;
+  float a_res = 0.f;
   const int nrb = (int)gridDim.y;
+  const float Rf = (float)p.R;
   for (int strip = blockIdx.x; strip < p.nstrips; strip += gridDim.x) {
     const int cl = tid & 63, part = tid >> 6;
     const int64_t col = (int64_t)strip * 64 + cl;
-    double acc = 0.0;
+    F2 acc{0.f, 0.f};
     float m1 = -FLT_MAX, m2 = FLT_MAX;
     if (col < p.C) {
-      for (int rb = part; rb < nrb; rb += 4) {
-        const float4 q = __ldcg(reinterpret_cast<const float4*>(p.part + (int64_t)rb * p.C + col));
-        acc += (double)q.x + (double)q.y;
-        m1 = fmaxf(m1, q.z);
-        m2 = fminf(m2, q.w);
+      for (int rb = part; rb < nrb; rb += 16) {
+        float4 q[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          q[j] = rb + 4 * j < nrb ? __ldcg(reinterpret_cast<const float4*>(p.part + (int64_t)(rb + 4 * j) * p.C + col))
+                                  : make_float4(0.f, 0.f, -FLT_MAX, FLT_MAX);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          acc = df_add(acc, F2{q[j].x, q[j].y});
+          m1 = fmaxf(m1, q[j].z);
+          m2 = fminf(m2, q[j].w);
+        }
       }
     }
     s_sum[part][cl] = acc;
@@ -289,14 +371,13 @@ __global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
     s_mn[part][cl] = m2;
     __syncthreads();
     if (tid < 64 && col < p.C) {
-      const double S = ((s_sum[0][cl] + s_sum[1][cl]) + s_sum[2][cl]) + s_sum[3][cl];
+      const F2 S = df_add(df_add(df_add(s_sum[0][cl], s_sum[1][cl]), s_sum[2][cl]), s_sum[3][cl]);
       const float M1 = fmaxf(fmaxf(s_mx[0][cl], s_mx[1][cl]), fmaxf(s_mx[2][cl], s_mx[3][cl]));
       const float M2 = fminf(fminf(s_mn[0][cl], s_mn[1][cl]), fminf(s_mn[2][cl], s_mn[3][cl]));
       if (p.split) {
-        const float mu = (float)(S / (double)p.R);
+        const float mu = df_div_count(S, Rf);
         p.mu[col] = mu;
         a_res = fmaxf(a_res, fmaxf(fabsf(__fsub_rn(M1, mu)), fabsf(__fsub_rn(M2, mu))));
-        a_mu = fmaxf(a_mu, fabsf(mu));
       } else {
         a_res = fmaxf(a_res, fmaxf(fabsf(M1), fabsf(M2)));
       }
@@ -305,65 +386,42 @@ __global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
   }
   if (tid == 0) p.ctrl[kCtrlStrip + blockIdx.x] = 0u;  // every row block has arrived: reset for the next call
   a_res = block_max256(a_res, red);
-  a_mu = block_max256(a_mu, red);
-  __threadfence();  // publish mu before taking the overall ticket
-  if (tid == 0) {
-    if (!p.hadamard) {
-      atomicMax(&p.ctrl[kCtrlAmaxRow], __float_as_uint(a_res));
-      atomicMax(&p.ctrl[kCtrlAmaxCol], __float_as_uint(a_res));
-    }
-    atomicMax(&p.ctrl[kCtrlAmaxMu], __float_as_uint(a_mu));
-    __threadfence();
-    const unsigned t = atomicAdd(&p.ctrl[kCtrlTicket], 1u);
-    s_last = (t == gridDim.x - 1);
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
+  if (tid == 0) atomicMax(&p.ctrl[kCtrlAmaxRes], __float_as_uint(a_res));
+}
 
-  // ---- last strip group overall: tensor scales, reset, quantize mu
-  __shared__ float s_amax_mu;
-  if (tid == 0) {
-    if (!p.hadamard) {
-      const float ar = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxRow], 0u));
-      const float ac = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxCol], 0u));
-      p.ctrl[kCtrlScaleRow] = __float_as_uint(tensor_scale_of(ar));
-      p.ctrl[kCtrlScaleCol] = __float_as_uint(tensor_scale_of(ac));
-    }
-    s_amax_mu = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxMu], 0u));
-    p.ctrl[kCtrlTicket] = 0u;
-    __threadfence();
-  }
-  __syncthreads();
-  if (!p.split) return;
-
-  // Quantize mu along C as one row ([1, C]).  Under the Hadamard variant mu
-  // is rotated block-wise first, and mu_hat is the dequantized mean rotated
-  // back (H16/4 is its own inverse).
-  const int64_t nb = p.C / 16;
-  float amax_mu = s_amax_mu;
-  if (p.hadamard) {
-    float a = 0.f;
-    for (int64_t b = tid; b < nb; b += 256) {
-      float v[16];
+// NVFP4 of the mean as one [1, C] row.  Under the Hadamard variant the mean
+// is rotated block-wise first, and mu_hat is the dequantized mean rotated
+// back (H16/4 is its own inverse).  The tensor scale comes from the maximum
+// magnitude of the (rotated) mean.  Run by one CTA of 256 threads.
+__device__ void quantize_mean(const float* mu, int64_t C, bool hadamard, uint8_t* mu_codes, uint8_t* mu_scales,
+                              float* mu_ts, float* mu_hat, int64_t kc, float* red) {
+  const int64_t nb = C / 16;
+  float a = 0.f;
+  for (int64_t b = threadIdx.x; b < nb; b += 256) {
+    float v[16];
 #pragma unroll
-      for (int e = 0; e < 16; ++e) v[e] = __ldcg(p.mu + 16 * b + e);
-      fwht16(v);
+    for (int e = 0; e < 16; ++e) v[e] = __ldcg(mu + 16 * b + e);
+    if (hadamard) fwht16(v);
 #pragma unroll
-      for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(v[e]));
-    }
-    amax_mu = block_max256(a, red);
+    for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(v[e]));
   }
-  const float s_g = tensor_scale_of(amax_mu);
-  if (tid == 0) *p.mu_ts = s_g;
+  const float s_g = tensor_scale_of(block_max256(a, red));
+  const int tid = threadIdx.x;
+  if (tid == 0) *mu_ts = s_g;
   for (int64_t b = tid; b < nb; b += 256) {
     float v[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = __ldcg(p.mu + 16 * b + e);
-    if (p.hadamard) fwht16(v);
+    for (int e = 0; e < 16; e += 4) {
+      const float4 m4 = __ldcg(reinterpret_cast<const float4*>(mu + 16 * b + e));
+      v[e] = m4.x;
+      v[e + 1] = m4.y;
+      v[e + 2] = m4.z;
+      v[e + 3] = m4.w;
+    }
+    if (hadamard) fwht16(v);
     const BlockQ q = quant_block16(v, s_g);
-    *reinterpret_cast<uint2*>(p.mu_codes + 8 * b) = make_uint2(q.lo, q.hi);
-    p.mu_scales[scale_offset(0, b, p.kc)] = (uint8_t)q.scale;
+    *reinterpret_cast<uint2*>(mu_codes + 8 * b) = make_uint2(q.lo, q.hi);
+    mu_scales[scale_offset(0, b, kc)] = (uint8_t)q.scale;
     const float sc = e4m3_value(q.scale);
     float d[16];
 #pragma unroll
@@ -371,19 +429,26 @@ __global__ void __launch_bounds__(256) colstats_kernel(StatsParams p) {
       const uint32_t c4 = ((e < 8 ? q.lo : q.hi) >> (4 * (e & 7))) & 15u;
       d[e] = __fmul_rn(__fmul_rn(e2m1_val(c4), sc), s_g);
     }
-    if (p.hadamard) fwht16(d);
+    if (hadamard) fwht16(d);
 #pragma unroll
-    for (int e = 0; e < 16; ++e) p.mu_hat[16 * b + e] = d[e];
+    for (int e = 0; e < 16; e += 4)
+      *reinterpret_cast<float4*>(mu_hat + 16 * b + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
   }
 }
 
 // ------------------------------------------------------------ pass 2 ----
 
 struct QuantParams {
-  const __nv_bfloat16* x;
   int64_t R, C;
   const float* mu;  // null: no split (r = x)
+  // quantized mean (split): [1, C]
+  uint8_t* mu_codes;
+  uint8_t* mu_scales;
+  float* mu_ts;
+  float* mu_hat;    // [C] dequantized, unrotated
+  int64_t mu_kc;    // ceil(C / 64)
   unsigned* ctrl;
+  int* err;
   int hadamard;
   // blocked along C: [R, C]
   uint8_t* row_codes;
@@ -400,227 +465,305 @@ struct QuantParams {
 
 constexpr int kQTile = 128;
 constexpr int kQThreads = 256;
-// smem: 2 x bf16 tile (64 KB) + column-layout code staging (8 KB) + scale staging (2 KB)
-constexpr int kQSmemTile = kQTile * kQTile * 2;
-constexpr int kQSmem = 2 * kQSmemTile + kQTile * 64 + 2048 + 64;
+constexpr int kQBufs = 3;                         // tile buffers per CTA
+constexpr int kQHalf = kQTile * 64 * 2;          // one 128-row x 64-column bf16 box (16 KB)
+constexpr int kQTileBytes = 2 * kQHalf;           // 32 KB
+// SMEM: tile buffers | mu [kQBufs][128] | inverse-scale tables [2][128] | column-layout scale atoms [1 KB] | barriers
+constexpr int kQOffMu = kQBufs * kQTileBytes;
+constexpr int kQOffInv = kQOffMu + kQBufs * 128 * 4;
+constexpr int kQOffCs = kQOffInv + 2 * 128 * 4;
+constexpr int kQOffBar = kQOffCs + 1024;
+constexpr int kQSmem = kQOffBar + 64 + 1024;      // + alignment slack
 
-// 16-byte chunk k (0..15) of a 256-byte tile row lives at chunk k ^ ((k >> 3) & 1):
-// row-wise 32-byte reads and column-wise reads are then conflict-free.
-__device__ __forceinline__ int qswz(int k) { return k ^ ((k >> 3) & 1); }
+// inv(e) = min(fl32(1 / fl32(e4m3(e) s_g)), FLT_MAX), or 0 when the decode scale is 0.
+__device__ __forceinline__ float inv_scale_of(uint32_t e, float s_g) {
+  const float sb = __fmul_rn(e4m3_value(e), s_g);
+  return sb > 0.f ? fminf(__frcp_rn(sb), FLT_MAX) : 0.f;
+}
 
-__device__ __forceinline__ void quant_issue_tile(const QuantParams& p, uint8_t* buf, int tile) {
-  const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
-  const int64_t r0 = (int64_t)tr * kQTile, c0 = (int64_t)tc * kQTile;
+__device__ __forceinline__ float absmax16(const float (&r)[16]) {
+  float a0 = 0.f, a1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int q = threadIdx.x + kQThreads * i;
-    const int row = q >> 4, k = q & 15;
-    const int64_t gr = r0 + row, gc = c0 + 8 * k;
-    const bool ok = gr < p.R && gc < p.C;
-    const __nv_bfloat16* src = ok ? p.x + gr * p.C + gc : p.x;
-    ptx::cp_async16(buf + row * 256 + qswz(k) * 16, src, ok ? 16u : 0u);
+  for (int e = 0; e < 16; e += 2) {
+    a0 = fmaxf(a0, fabsf(r[e]));
+    a1 = fmaxf(a1, fabsf(r[e + 1]));
+  }
+  return fmaxf(a0, a1);
+}
+
+// NVFP4 of one 16-element block with a per-tensor table of reciprocal decode
+// scales (same binary32 steps as quant_block16).  Returns the E4M3 code.
+__device__ __forceinline__ uint32_t quant16_tab(const float (&r)[16], float den, bool s_pos, const float* inv_tab,
+                                                uint32_t& lo, uint32_t& hi) {
+  const float a = absmax16(r);
+  const uint32_t code = s_pos ? ptx::cvt_e4m3(__fdiv_rn(a, den)) : 0u;
+  const float inv = inv_tab[code];
+  const uint64_t inv2 = f2pack(inv, inv);
+  uint32_t w[2] = {0u, 0u};
+#pragma unroll
+  for (int e = 0; e < 8; ++e) {
+    const uint64_t q = mul2(f2pack(r[2 * e], r[2 * e + 1]), inv2);
+    w[e >> 2] |= ptx::cvt_e2m1x2(f2lo(q), f2hi(q)) << (8 * (e & 3));
+  }
+  lo = w[0];
+  hi = w[1];
+  return code;
+}
+
+// Blocks along C (row layout).  Warps 0-3; lane = (block pair bq = lane / 8,
+// row rr = 8 * warp + lane % 8): blocks 2bq, 2bq+1 (tile columns 32bq..32bq+31)
+// of tile rows rr, rr+32, rr+64, rr+96.  The tile sits in SMEM as two
+// 64-column halves of 128 rows x 128 bytes, 16-byte chunk j of row r at chunk
+// j ^ (r % 8) (the TMA 128-byte swizzle): the 8 lanes of a load phase read 8
+// different rows at distinct banks.
+template <bool AMAX_ONLY>
+__device__ __forceinline__ void quant_rows(const QuantParams& p, const uint8_t* buf, const float* mu_s, int64_t r0,
+                                           int64_t c0, int tr, int tc, bool split, float den, bool s_pos,
+                                           const float* inv_tab, float& amax) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int bq = lane >> 3, rr = 8 * warp + (lane & 7);
+  const uint8_t* half = buf + (bq >> 1) * kQHalf;
+  const int ch0 = 4 * (bq & 1);
+  float m[32];
+#pragma unroll
+  for (int k = 0; k < 32; k += 4) {
+    const float4 m4 = split ? *reinterpret_cast<const float4*>(mu_s + 32 * bq + k) : make_float4(0.f, 0.f, 0.f, 0.f);
+    m[k] = m4.x;
+    m[k + 1] = m4.y;
+    m[k + 2] = m4.z;
+    m[k + 3] = m4.w;
+  }
+  const bool cvalid0 = c0 + 32 * bq < p.C, cvalid1 = c0 + 32 * bq + 16 < p.C;
+#pragma unroll 1
+  for (int pp = 0; pp < 4; ++pp) {
+    const int row = rr + 32 * pp;
+    const int64_t gr = r0 + row;
+    const bool rvalid = gr < p.R;
+    uint4 v[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const uint4*>(half + row * 128 + (((ch0 + k) ^ (row & 7)) << 4));
+    uint32_t code[4];
+    uint32_t sc = 0;
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+      const uint32_t wv[8] = {v[2 * b].x, v[2 * b].y, v[2 * b].z, v[2 * b].w,
+                              v[2 * b + 1].x, v[2 * b + 1].y, v[2 * b + 1].z, v[2 * b + 1].w};
+      float rx[16];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const uint64_t d = split ? sub2(bf2_to_f2(wv[e]), f2pack(m[16 * b + 2 * e], m[16 * b + 2 * e + 1]))
+                                 : bf2_to_f2(wv[e]);
+        rx[2 * e] = f2lo(d);
+        rx[2 * e + 1] = f2hi(d);
+      }
+      if (!rvalid || !(b ? cvalid1 : cvalid0)) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) rx[e] = 0.f;
+      }
+      if (p.hadamard) fwht16(rx);
+      if (AMAX_ONLY) {
+        amax = fmaxf(amax, absmax16(rx));
+      } else {
+        sc |= quant16_tab(rx, den, s_pos, inv_tab, code[2 * b], code[2 * b + 1]) << (8 * b);
+      }
+    }
+    if (AMAX_ONLY) continue;
+    const int64_t boff = c0 / 2 + 16 * bq;
+    if (rvalid && boff < p.row_ld)
+      *reinterpret_cast<uint4*>(p.row_codes + gr * p.row_ld + boff) = make_uint4(code[0], code[1], code[2], code[3]);
+    const int64_t kc = 2 * (int64_t)tc + (bq >> 1);
+    if (kc < p.row_kc)
+      *reinterpret_cast<uint16_t*>(p.row_scales + ((int64_t)tr * p.row_kc + kc) * 512 + 16 * (row & 31) +
+                                   4 * (row >> 5) + 2 * (bq & 1)) = (uint16_t)sc;
   }
 }
 
-// AMAX_ONLY: compute the rotated residual's per-layout maximum magnitude
-// (Hadamard variant) instead of quantizing.
+// Blocks along R (column layout): warp w (4..7 -> 0..3) owns tile columns
+// 32w..32w+31; lane = (column quad cq = lane % 8, row block rbl = lane / 8);
+// two units per lane (row blocks rbl and rbl + 4), each 4 columns x 16 rows.
+// Codes go straight to global memory (4 lanes fill one 32-byte sector),
+// block scales to the SMEM atom staging `cs`.
 template <bool AMAX_ONLY>
-__global__ void __launch_bounds__(kQThreads, 2) split_quant_kernel(QuantParams p) {
-  extern __shared__ __align__(128) uint8_t qsm[];
-  uint8_t* cstage = qsm + 2 * kQSmemTile;                 // [128 rows][64 B], 8-byte granules swizzled
-  uint8_t* sstage_row = cstage + kQTile * 64;             // 1 KB: 2 scale chunks of the row layout
-  uint8_t* sstage_col = sstage_row + 1024;                // 1 KB: 2 scale chunks of the column layout
+__device__ __forceinline__ void quant_cols(const QuantParams& p, const uint8_t* buf, const float* mu_s, int64_t r0,
+                                           int64_t c0, bool split, float den, bool s_pos, const float* inv_tab,
+                                           uint8_t* cs, float& amax) {
+  const int w = (threadIdx.x >> 5) - 4, lane = threadIdx.x & 31;
+  const int cq = lane & 7, rbl = lane >> 3;
+  const int cc0 = 32 * w + 4 * cq;                       // first of this lane's 4 tile columns
+  const uint8_t* half = buf + (w >> 1) * kQHalf;
+  const int c16 = 4 * (w & 1) + (cq >> 1), sub = 8 * (cq & 1);
+  float m[4] = {0.f, 0.f, 0.f, 0.f};
+  if (split) {
+    const float4 m4 = *reinterpret_cast<const float4*>(mu_s + cc0);
+    m[0] = m4.x;
+    m[1] = m4.y;
+    m[2] = m4.z;
+    m[3] = m4.w;
+  }
+#pragma unroll 1
+  for (int u = 0; u < 2; ++u) {
+    const int rb = rbl + 4 * u;
+    const bool rows_partial = r0 + 16 * rb + 16 > p.R;
+    uint2 x[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      const int row = 16 * rb + e;
+      x[e] = *reinterpret_cast<const uint2*>(half + row * 128 + ((c16 ^ (row & 7)) << 4) + sub);
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float rx[16];
+#pragma unroll
+      for (int e = 0; e < 16; e += 2) {
+        const uint32_t wa = (j >> 1) ? x[e].y : x[e].x;
+        const uint32_t wb = (j >> 1) ? x[e + 1].y : x[e + 1].x;
+        const float xa = (j & 1) ? bf16hi(wa) : bf16lo(wa);
+        const float xb = (j & 1) ? bf16hi(wb) : bf16lo(wb);
+        if (split) {
+          const uint64_t d = sub2(f2pack(xa, xb), f2pack(m[j], m[j]));
+          rx[e] = f2lo(d);
+          rx[e + 1] = f2hi(d);
+        } else {
+          rx[e] = xa;
+          rx[e + 1] = xb;
+        }
+      }
+      const int cc = cc0 + j;
+      const bool cvalid = c0 + cc < p.C;
+      if (!cvalid) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) rx[e] = 0.f;
+      } else if (rows_partial) {
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (r0 + 16 * rb + e >= p.R) rx[e] = 0.f;
+      }
+      if (p.hadamard) fwht16(rx);
+      if (AMAX_ONLY) {
+        amax = fmaxf(amax, absmax16(rx));
+      } else {
+        uint32_t lo, hi;
+        const uint32_t s = quant16_tab(rx, den, s_pos, inv_tab, lo, hi);
+        const int64_t off = r0 / 2 + 8 * rb;
+        if (cvalid && off < p.col_ld)
+          *reinterpret_cast<uint2*>(p.col_codes + (c0 + cc) * p.col_ld + off) = make_uint2(lo, hi);
+        cs[(rb >> 2) * 512 + 16 * (cc & 31) + 4 * (cc >> 5) + (rb & 3)] = (uint8_t)s;
+      }
+    }
+  }
+}
+
+// Split + quantize, both layouts from one read of each 128 x 128 tile.
+// Persistent CTAs with kQBufs tile buffers filled by TMA (mbarrier-tracked);
+// warps 0-3 write the row layout and warps 4-7 the column layout of the
+// same tile; the last CTA also quantizes the mean, and the last CTA to finish
+// resets the control block's maxima.  AMAX_ONLY: compute the rotated
+// residual's per-layout maximum magnitude (Hadamard variant) instead of
+// quantizing.
+template <bool AMAX_ONLY>
+__global__ void __launch_bounds__(kQThreads, 2)
+    split_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
+  extern __shared__ uint8_t qraw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
+  float* mu_s = reinterpret_cast<float*>(sm + kQOffMu);
+  float* inv_s = reinterpret_cast<float*>(sm + kQOffInv);
+  uint8_t* cs = sm + kQOffCs;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kQOffBar);
   __shared__ float red[8];
+  __shared__ int s_flag;
 
-  __shared__ int s_last;
-
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int ntiles = p.tiles_r * p.tiles_c;
   const bool split = p.mu != nullptr;
+  const bool rows_on = AMAX_ONLY || p.row_codes != nullptr;
+  const bool cols_on = AMAX_ONLY || p.col_codes != nullptr;
 
-  // the input was written before the previous kernel started: fetch the
-  // first tile while that kernel finishes
-  int buf = 0;
-  if ((int)blockIdx.x < ntiles) quant_issue_tile(p, qsm, blockIdx.x);
-  ptx::cp_async_commit();
+  auto issue = [&](int tile, int b) {
+    const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
+    ptx::mbar_arrive_expect_tx(&full[b], (uint32_t)kQTileBytes);
+    ptx::tma_load_2d(sm + b * kQTileBytes, &tmX, tc * kQTile, tr * kQTile, &full[b]);
+    ptx::tma_load_2d(sm + b * kQTileBytes + kQHalf, &tmX, tc * kQTile + 64, tr * kQTile, &full[b]);
+  };
+  if (tid == 0) {
+    for (int b = 0; b < kQBufs; ++b) ptx::mbar_init(&full[b], 1);
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmX);
+    // the input was written before the previous kernel started: fetch while it finishes
+    for (int b = 0; b < kQBufs; ++b)
+      if ((int)(blockIdx.x + b * gridDim.x) < ntiles) issue(blockIdx.x + b * gridDim.x, b);
+  }
   ptx::pdl_wait_and_release();
 
-  const float s_row = AMAX_ONLY ? 0.f : __uint_as_float(__ldcg(&p.ctrl[kCtrlScaleRow]));
-  const float s_col = AMAX_ONLY ? 0.f : __uint_as_float(__ldcg(&p.ctrl[kCtrlScaleCol]));
-  if (!AMAX_ONLY && blockIdx.x == 0 && threadIdx.x == 0) {
-    if (p.row_ts) *p.row_ts = s_row;
-    if (p.col_ts) *p.col_ts = s_col;
+  float s_row = 0.f, s_col = 0.f;
+  if (!AMAX_ONLY) {
+    // tensor scales from the maxima of the stats pass (or of the rotated-maximum pass)
+    s_row = tensor_scale_of(__uint_as_float(__ldcg(&p.ctrl[p.hadamard ? kCtrlAmaxRowH : kCtrlAmaxRes])));
+    s_col = tensor_scale_of(__uint_as_float(__ldcg(&p.ctrl[p.hadamard ? kCtrlAmaxColH : kCtrlAmaxRes])));
+    if (tid < 128) {
+      inv_s[tid] = tid < 127 ? inv_scale_of(tid, s_row) : 0.f;
+      inv_s[128 + tid] = tid < 127 ? inv_scale_of(tid, s_col) : 0.f;
+    }
+    if (blockIdx.x == 0 && tid == 0) {
+      if (p.row_ts) *p.row_ts = s_row;
+      if (p.col_ts) *p.col_ts = s_col;
+    }
   }
+  const float den_row = __fmul_rn(6.0f, s_row), den_col = __fmul_rn(6.0f, s_col);
   float amax_row = 0.f, amax_col = 0.f;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int next = tile + gridDim.x;
-    if (next < ntiles) quant_issue_tile(p, qsm + (buf ^ 1) * kQSmemTile, next);
-    ptx::cp_async_commit();
-    ptx::cp_async_wait<1>();
-    __syncthreads();
+  if (!AMAX_ONLY && split && blockIdx.x == gridDim.x - 1)
+    quantize_mean(p.mu, p.C, p.hadamard != 0, p.mu_codes, p.mu_scales, p.mu_ts, p.mu_hat, p.mu_kc, red);
 
+  int i = 0;
+  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+    const int b = i % kQBufs;
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     const int64_t r0 = (int64_t)tr * kQTile, c0 = (int64_t)tc * kQTile;
-    const uint8_t* t = qsm + buf * kQSmemTile;
-
-    // ---- blocks along C (row layout): thread = (row, 16-column block), 4 per thread
-    if (p.row_codes != nullptr || AMAX_ONLY) {
-#pragma unroll 1
-      for (int i = 0; i < 4; ++i) {
-        const int row = warp * 4 + (lane >> 3) + 32 * i;
-        const int kb = lane & 7;
-        const int64_t gr = r0 + row, gc = c0 + 16 * kb;
-        const bool valid = gr < p.R && gc < p.C;
-        const uint4 v0 = *reinterpret_cast<const uint4*>(t + row * 256 + qswz(2 * kb) * 16);
-        const uint4 v1 = *reinterpret_cast<const uint4*>(t + row * 256 + qswz(2 * kb + 1) * 16);
-        const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-        float r[16];
-        if (valid) {
-          if (split) {
-            const float4* mp = reinterpret_cast<const float4*>(p.mu + gc);
-            float mu[16];
-#pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              const float4 m4 = __ldg(mp + q4);
-              mu[4 * q4] = m4.x;
-              mu[4 * q4 + 1] = m4.y;
-              mu[4 * q4 + 2] = m4.z;
-              mu[4 * q4 + 3] = m4.w;
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              r[2 * e] = __fsub_rn(bf16lo(wv[e]), mu[2 * e]);
-              r[2 * e + 1] = __fsub_rn(bf16hi(wv[e]), mu[2 * e + 1]);
-            }
-          } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-              r[2 * e] = bf16lo(wv[e]);
-              r[2 * e + 1] = bf16hi(wv[e]);
-            }
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) r[e] = 0.f;
-        }
-        if (p.hadamard) fwht16(r);
-        if (AMAX_ONLY) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) amax_row = fmaxf(amax_row, fabsf(r[e]));
-        } else {
-          const BlockQ q = quant_block16(r, s_row);
-          if (valid) *reinterpret_cast<uint2*>(p.row_codes + gr * p.row_ld + c0 / 2 + 8 * kb) = make_uint2(q.lo, q.hi);
-          sstage_row[(kb >> 2) * 512 + 16 * (row & 31) + 4 * (row >> 5) + (kb & 3)] = (uint8_t)q.scale;
-        }
-      }
-    }
-
-    // ---- blocks along R (column layout): thread = (2 columns, 16-row block), 2 per thread
-    if (p.col_codes != nullptr || AMAX_ONLY) {
-#pragma unroll 1
-      for (int i = 0; i < 2; ++i) {
-        const int cp = lane + 32 * (warp & 1);         // column pair 0..63
-        const int rb = (warp >> 1) + 4 * i;            // 16-row block 0..7
-        const int col = 2 * cp;
-        const int64_t gc = c0 + col;
-        const bool cvalid = gc < p.C;
-        float mu0 = 0.f, mu1 = 0.f;
-        if (split && cvalid) {
-          const float2 m2 = __ldg(reinterpret_cast<const float2*>(p.mu + gc));
-          mu0 = m2.x;
-          mu1 = m2.y;
-        }
-        float ra[16], rbv[16];
-        const int choff = qswz(col >> 3) * 16 + (col & 7) * 2;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int row = 16 * rb + e;
-          const uint32_t w = *reinterpret_cast<const uint32_t*>(t + row * 256 + choff);
-          const bool valid = cvalid && (r0 + row < p.R);
-          if (valid) {
-            ra[e] = split ? __fsub_rn(bf16lo(w), mu0) : bf16lo(w);
-            rbv[e] = split ? __fsub_rn(bf16hi(w), mu1) : bf16hi(w);
-          } else {
-            ra[e] = 0.f;
-            rbv[e] = 0.f;
-          }
-        }
-        if (p.hadamard) {
-          fwht16(ra);
-          fwht16(rbv);
-        }
-        if (AMAX_ONLY) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) amax_col = fmaxf(amax_col, fmaxf(fabsf(ra[e]), fabsf(rbv[e])));
-        } else {
-          const BlockQ qa = quant_block16(ra, s_col);
-          const BlockQ qb = quant_block16(rbv, s_col);
-          *reinterpret_cast<uint2*>(cstage + col * 64 + 8 * (rb ^ (col & 7))) = make_uint2(qa.lo, qa.hi);
-          *reinterpret_cast<uint2*>(cstage + (col + 1) * 64 + 8 * (rb ^ ((col + 1) & 7))) = make_uint2(qb.lo, qb.hi);
-          sstage_col[(rb >> 2) * 512 + 16 * (col & 31) + 4 * (col >> 5) + (rb & 3)] = (uint8_t)qa.scale;
-          sstage_col[(rb >> 2) * 512 + 16 * ((col + 1) & 31) + 4 * ((col + 1) >> 5) + (rb & 3)] = (uint8_t)qb.scale;
-        }
-      }
-    }
+    float* mub = mu_s + 128 * b;
+    if (tid < 128) mub[tid] = (split && c0 + tid < p.C) ? __ldg(p.mu + c0 + tid) : 0.f;
+    if (tid == 0) s_flag = ptx::mbar_wait(&full[b], (uint32_t)((i / kQBufs) & 1), kWaitLimit) ? 1 : 0;
     __syncthreads();
-
-    if (!AMAX_ONLY) {
-      // column-layout codes: row (c0 + c) bytes r0/2 .. r0/2+63, four 8-byte granules per thread
-      if (p.col_codes != nullptr) {
-        const int c = threadIdx.x >> 1, half = threadIdx.x & 1;
-        const int64_t grow = c0 + c;
-        if (grow < p.C) {
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int64_t boff = r0 / 2 + 32 * half + 16 * h;
-            if (boff < p.col_ld) {
-              const int g0 = 4 * half + 2 * h;
-              const uint2 a = *reinterpret_cast<const uint2*>(cstage + c * 64 + 8 * (g0 ^ (c & 7)));
-              const uint2 b = *reinterpret_cast<const uint2*>(cstage + c * 64 + 8 * ((g0 + 1) ^ (c & 7)));
-              *reinterpret_cast<uint4*>(p.col_codes + grow * p.col_ld + boff) = make_uint4(a.x, a.y, b.x, b.y);
-            }
-          }
-        }
-        // scale chunks of the column layout: row chunk tc, chunks 2*tr, 2*tr+1
-        if (threadIdx.x < 64) {
-          const int ch = threadIdx.x >> 5;
-          const int64_t kc = 2 * (int64_t)tr + ch;
-          if (kc < p.col_kc)
-            *reinterpret_cast<uint4*>(p.col_scales + ((int64_t)tc * p.col_kc + kc) * 512 + 16 * (threadIdx.x & 31)) =
-                *reinterpret_cast<const uint4*>(sstage_col + 16 * threadIdx.x);
-        }
-      }
-      if (p.row_codes != nullptr && threadIdx.x >= 64 && threadIdx.x < 128) {
-        const int tt = threadIdx.x - 64, ch = tt >> 5;
-        const int64_t kc = 2 * (int64_t)tc + ch;
-        if (kc < p.row_kc)
-          *reinterpret_cast<uint4*>(p.row_scales + ((int64_t)tr * p.row_kc + kc) * 512 + 16 * (tt & 31)) =
-              *reinterpret_cast<const uint4*>(sstage_row + 16 * tt);
-      }
-      __syncthreads();
+    if (!s_flag) {
+      if (tid == 0) atomicExch(p.err, kErrQuantLoad);
+      break;
     }
-    buf ^= 1;
+    const uint8_t* buf = sm + b * kQTileBytes;
+    if (warp < 4) {
+      if (rows_on) quant_rows<AMAX_ONLY>(p, buf, mub, r0, c0, tr, tc, split, den_row, s_row > 0.f, inv_s, amax_row);
+    } else if (cols_on) {
+      quant_cols<AMAX_ONLY>(p, buf, mub, r0, c0, split, den_col, s_col > 0.f, inv_s + 128, cs, amax_col);
+    }
+    __syncthreads();  // the tile buffer and the scale staging are complete
+    if (tid == 0 && tile + kQBufs * (int)gridDim.x < ntiles) issue(tile + kQBufs * gridDim.x, b);
+    if (!AMAX_ONLY && p.col_codes != nullptr && tid < 64) {
+      // column-layout scale atoms: row chunk tc, chunks 2*tr and 2*tr + 1
+      const int64_t kc = 2 * (int64_t)tr + (tid >> 5);
+      if (kc < p.col_kc)
+        *reinterpret_cast<uint4*>(p.col_scales + ((int64_t)tc * p.col_kc + kc) * 512 + 16 * (tid & 31)) =
+            *reinterpret_cast<const uint4*>(cs + 16 * tid);
+    }
   }
-  ptx::cp_async_wait<0>();
   if (AMAX_ONLY) {
-    // rotated maxima -> tensor scales; the last CTA converts and resets
+    // rotated maxima, read by the quantize pass that follows
     amax_row = block_max256(amax_row, red);
     amax_col = block_max256(amax_col, red);
-    if (threadIdx.x == 0) {
-      atomicMax(&p.ctrl[kCtrlAmaxRow], __float_as_uint(amax_row));
-      atomicMax(&p.ctrl[kCtrlAmaxCol], __float_as_uint(amax_col));
-      __threadfence();
-      const unsigned t = atomicAdd(&p.ctrl[kCtrlAmaxTicket], 1u);
-      s_last = (t == gridDim.x - 1);
+    if (tid == 0) {
+      atomicMax(&p.ctrl[kCtrlAmaxRowH], __float_as_uint(amax_row));
+      atomicMax(&p.ctrl[kCtrlAmaxColH], __float_as_uint(amax_col));
     }
+  } else {
+    // every CTA has read the maxima: the last one to finish resets them
+    __shared__ int s_last;
     __syncthreads();
-    if (s_last && threadIdx.x == 0) {
+    if (tid == 0) {
       __threadfence();
-      const float ar = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxRow], 0u));
-      const float ac = __uint_as_float(atomicExch(&p.ctrl[kCtrlAmaxCol], 0u));
-      p.ctrl[kCtrlScaleRow] = __float_as_uint(tensor_scale_of(ar));
-      p.ctrl[kCtrlScaleCol] = __float_as_uint(tensor_scale_of(ac));
-      p.ctrl[kCtrlAmaxTicket] = 0u;
+      const unsigned t = atomicAdd(&p.ctrl[kCtrlQuantTicket], 1u);
+      s_last = (t == gridDim.x - 1);
+      if (s_last) {
+        p.ctrl[kCtrlAmaxRes] = 0u;
+        p.ctrl[kCtrlAmaxRowH] = 0u;
+        p.ctrl[kCtrlAmaxColH] = 0u;
+        p.ctrl[kCtrlQuantTicket] = 0u;
+      }
     }
   }
 }
