@@ -153,9 +153,16 @@ bool nvfp4_ok(const averis_nvfp4* t, int64_t rows, int64_t cols) {
 
 // ------------------------------------------------------------- quantize --
 
+// Largest column count of a mean split: the NVFP4 mean is staged in the
+// shared memory of the quantize pass's mean CTAs.
+constexpr int64_t kMaxSplitCols = 147456;
+
+// r_w / r_out (optional, split only): also compute the rank-one row
+// r_out[N] = deq(mu_q) deq(r_w)^T for an NVFP4 r_w [N, C] blocked along C.
 averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags, float* mu, const averis_nvfp4* mu_q,
                             float* mu_hat, const averis_nvfp4* out_row, const averis_nvfp4* out_col, void* ws,
-                            size_t ws_bytes, cudaStream_t s) {
+                            size_t ws_bytes, cudaStream_t s, const averis_nvfp4* r_w = nullptr,
+                            float* r_out = nullptr) {
   if (x == nullptr || R < 1 || C < 16 || C % 16 != 0 || !aligned(x, 16)) return AVERIS_ERR_INVALID_ARG;
   if (R > (int64_t)1 << 31 || C > (int64_t)1 << 31) return AVERIS_ERR_INVALID_ARG;
   const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
@@ -164,6 +171,10 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   if (out_col != nullptr && !nvfp4_ok(out_col, C, R)) return AVERIS_ERR_INVALID_ARG;
   if (split && (mu == nullptr || mu_hat == nullptr || !aligned(mu, 16) || !aligned(mu_hat, 16) ||
                 !nvfp4_ok(mu_q, 1, C)))
+    return AVERIS_ERR_INVALID_ARG;
+  if (split && C > kMaxSplitCols) return AVERIS_ERR_INVALID_ARG;
+  if ((r_w == nullptr) != (r_out == nullptr)) return AVERIS_ERR_INVALID_ARG;
+  if (r_w != nullptr && (!split || r_w->rows < 1 || !nvfp4_ok(r_w, r_w->rows, C) || !aligned(r_out, 4)))
     return AVERIS_ERR_INVALID_ARG;
   if (ws == nullptr || !aligned(ws, 256)) return AVERIS_ERR_INVALID_ARG;
   if (ws_bytes < quant_ws_bytes(R, C)) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
@@ -235,11 +246,35 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
       return AVERIS_ERR_CUDA;
   }
   if (out_row == nullptr && out_col == nullptr) qp.tiles_r = 0;  // mean only
+  // mean CTAs: one for the mean alone, more when they also compute the
+  // rank-one row (about 256 K weights each, at most 32)
+  qp.mean_ctas = 0;
+  if (split) {
+    qp.mean_ctas = 1;
+    if (r_w != nullptr) {
+      qp.w_codes = r_w->codes;
+      qp.w_scales = r_w->scales;
+      qp.w_ts = r_w->tensor_scale;
+      qp.w_rows = r_w->rows;
+      qp.w_ld = averis_nvfp4_ld(C);
+      qp.w_kc = cdiv(C, 64);
+      qp.r_out = r_out;
+      qp.mean_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(32, cdiv(r_w->rows * C, (int64_t)1 << 18)));
+    }
+  }
   const int ntiles = qp.tiles_r * qp.tiles_c;
-  const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, 2 * (int64_t)dev->sms));
-  if (had && launch_pdl(split_quant_kernel<true>, dim3(grid), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess)
-    return AVERIS_ERR_CUDA;
-  if (launch_pdl(split_quant_kernel<false>, dim3(grid), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess)
+  // all CTAs resident at once (2 per SM): tile CTAs fill what the mean CTAs leave
+  const int tile_ctas =
+      ntiles == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, 2 * (int64_t)dev->sms - qp.mean_ctas));
+  if (had) {
+    QuantParams ap = qp;  // rotated-maximum pass: tiles only
+    ap.mean_ctas = 0;
+    if (launch_pdl(split_quant_kernel<true>, dim3(std::max(1, tile_ctas)), dim3(kQThreads), kQSmem, s, tx, ap) !=
+        cudaSuccess)
+      return AVERIS_ERR_CUDA;
+  }
+  if (launch_pdl(split_quant_kernel<false>, dim3(std::max(1, qp.mean_ctas + tile_ctas)), dim3(kQThreads), kQSmem, s,
+                 tx, qp) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }
@@ -371,11 +406,8 @@ averis_status linear_fwd_impl(const void* x, int64_t l, int64_t m, int64_t n, co
   void* qws = c.take(quant_ws_bytes(l, m));
   float* r_x = static_cast<float*>(c.take((size_t)n * 4));
   averis_status r = quantize_impl(x, l, m, flags, st->mu, &st->mu_q, st->mu_hat, &st->x_row, &st->x_col, qws,
-                                  quant_ws_bytes(l, m), s);
+                                  quant_ws_bytes(l, m), s, split ? w_m : nullptr, split ? r_x : nullptr);
   if (r != AVERIS_OK) return r;
-  if (split) {
-    if ((r = rank1_impl(&st->mu_q, w_m, r_x, s)) != AVERIS_OK) return r;
-  }
   return gemm_impl(&st->x_row, w_m, split ? r_x : nullptr, nullptr, nullptr, 0.f, y, n, flags, s);
 }
 
@@ -397,11 +429,9 @@ averis_status linear_bwd_impl(const void* d, int64_t l, int64_t m, int64_t n, co
   float* mu = static_cast<float*>(c.take((size_t)n * 4));
   float* mu_hat = static_cast<float*>(c.take((size_t)n * 4));
   float* r_d = static_cast<float*>(c.take((size_t)m * 4));
-  averis_status r = quantize_impl(d, l, n, flags, mu, &mu_q, mu_hat, &d_row, &d_col, qws, quant_ws_bytes(l, n), s);
+  averis_status r = quantize_impl(d, l, n, flags, mu, &mu_q, mu_hat, &d_row, &d_col, qws, quant_ws_bytes(l, n), s,
+                                  split ? w_n : nullptr, split ? r_d : nullptr);
   if (r != AVERIS_OK) return r;
-  if (split) {
-    if ((r = rank1_impl(&mu_q, w_n, r_d, s)) != AVERIS_OK) return r;
-  }
   if ((r = gemm_impl(&d_row, w_n, split ? r_d : nullptr, nullptr, nullptr, 0.f, dx, m, flags, s)) != AVERIS_OK)
     return r;
   return gemm_impl(&st->x_col, &d_col, nullptr, split ? st->mu_hat : nullptr, split ? mu_hat : nullptr, (float)l, dw,

@@ -23,6 +23,7 @@
 #include <cfloat>
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "ptx.cuh"
 
@@ -389,39 +390,45 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
   if (tid == 0) atomicMax(&p.ctrl[kCtrlAmaxRes], __float_as_uint(a_res));
 }
 
-// NVFP4 of the mean as one [1, C] row.  Under the Hadamard variant the mean
-// is rotated block-wise first, and mu_hat is the dequantized mean rotated
-// back (H16/4 is its own inverse).  The tensor scale comes from the maximum
-// magnitude of the (rotated) mean.  Run by one CTA of 256 threads.
-__device__ void quantize_mean(const float* mu, int64_t C, bool hadamard, uint8_t* mu_codes, uint8_t* mu_scales,
-                              float* mu_ts, float* mu_hat, int64_t kc, float* red) {
-  const int64_t nb = C / 16;
+// NVFP4 of the mean as one [1, C] row, into SMEM (codes: C/2 bytes, one E4M3
+// byte per block) and, when `p.mu_codes` is to be written by this CTA, into
+// the caller's tensor (codes, tiled scales, tensor scale) and mu_hat.  Under
+// the Hadamard variant the mean is rotated block-wise first, and mu_hat is
+// the dequantized mean rotated back (H16/4 is its own inverse).  The tensor
+// scale comes from the maximum magnitude of the (rotated) mean.  All 256
+// threads of the CTA take part; returns the tensor scale.
+template <typename P>
+__device__ float quantize_mean(const P& p, bool write_global, uint8_t* s_codes, uint8_t* s_scales, float* red) {
+  const int64_t nb = p.C / 16;
+  const bool had = p.hadamard != 0;
   float a = 0.f;
   for (int64_t b = threadIdx.x; b < nb; b += 256) {
     float v[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = __ldcg(mu + 16 * b + e);
-    if (hadamard) fwht16(v);
+    for (int e = 0; e < 16; ++e) v[e] = __ldcg(p.mu + 16 * b + e);
+    if (had) fwht16(v);
 #pragma unroll
     for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(v[e]));
   }
   const float s_g = tensor_scale_of(block_max256(a, red));
-  const int tid = threadIdx.x;
-  if (tid == 0) *mu_ts = s_g;
-  for (int64_t b = tid; b < nb; b += 256) {
+  if (write_global && threadIdx.x == 0) *p.mu_ts = s_g;
+  for (int64_t b = threadIdx.x; b < nb; b += 256) {
     float v[16];
 #pragma unroll
     for (int e = 0; e < 16; e += 4) {
-      const float4 m4 = __ldcg(reinterpret_cast<const float4*>(mu + 16 * b + e));
+      const float4 m4 = __ldcg(reinterpret_cast<const float4*>(p.mu + 16 * b + e));
       v[e] = m4.x;
       v[e + 1] = m4.y;
       v[e + 2] = m4.z;
       v[e + 3] = m4.w;
     }
-    if (hadamard) fwht16(v);
+    if (had) fwht16(v);
     const BlockQ q = quant_block16(v, s_g);
-    *reinterpret_cast<uint2*>(mu_codes + 8 * b) = make_uint2(q.lo, q.hi);
-    mu_scales[scale_offset(0, b, kc)] = (uint8_t)q.scale;
+    *reinterpret_cast<uint2*>(s_codes + 8 * b) = make_uint2(q.lo, q.hi);
+    s_scales[b] = (uint8_t)q.scale;
+    if (!write_global) continue;
+    *reinterpret_cast<uint2*>(p.mu_codes + 8 * b) = make_uint2(q.lo, q.hi);
+    p.mu_scales[scale_offset(0, b, p.mu_kc)] = (uint8_t)q.scale;
     const float sc = e4m3_value(q.scale);
     float d[16];
 #pragma unroll
@@ -429,10 +436,79 @@ __device__ void quantize_mean(const float* mu, int64_t C, bool hadamard, uint8_t
       const uint32_t c4 = ((e < 8 ? q.lo : q.hi) >> (4 * (e & 7))) & 15u;
       d[e] = __fmul_rn(__fmul_rn(e2m1_val(c4), sc), s_g);
     }
-    if (hadamard) fwht16(d);
+    if (had) fwht16(d);
 #pragma unroll
     for (int e = 0; e < 16; e += 4)
-      *reinterpret_cast<float4*>(mu_hat + 16 * b + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+      *reinterpret_cast<float4*>(p.mu_hat + 16 * b + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+  }
+  __syncthreads();
+  return s_g;
+}
+
+// The four bytes of a code word (eight E2M1 codes) as four f16 pairs.  E2M1
+// values are exact in f16, and a dot product does not depend on the order
+// of the pair halves, so the two operands just have to be unpacked alike.
+__device__ __forceinline__ void e2m1x8_to_h2(uint32_t w, uint32_t (&h)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+      : "r"(w));
+}
+
+// Sum of the 16 products of two NVFP4 code blocks (two words each).  Each
+// product of E2M1 values is a multiple of 1/4 of magnitude <= 36, and each
+// f16 half accumulates 8 of them (<= 288, 1152 quarter units < 2^11): every
+// step is exact in f16, and the final binary32 sum is exact too.
+__device__ __forceinline__ float dot16_codes(uint2 a, uint2 b) {
+  uint32_t ha[4], hb[4];
+  __half2 acc = __float2half2_rn(0.f);
+  e2m1x8_to_h2(a.x, ha);
+  e2m1x8_to_h2(b.x, hb);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    acc = __hfma2(*reinterpret_cast<__half2*>(&ha[k]), *reinterpret_cast<__half2*>(&hb[k]), acc);
+  e2m1x8_to_h2(a.y, ha);
+  e2m1x8_to_h2(b.y, hb);
+#pragma unroll
+  for (int k = 0; k < 4; ++k)
+    acc = __hfma2(*reinterpret_cast<__half2*>(&ha[k]), *reinterpret_cast<__half2*>(&hb[k]), acc);
+  const float2 f = __half22float2(acc);
+  return f.x + f.y;
+}
+
+// Rank-one row r[n] = s_mu s_w sum_k deq(mu)_k deq(W)_{n,k} for rows
+// [n0, n1) of W, with the NVFP4 mean in SMEM.  Warp per row, lanes over
+// 32-element chunks; block products in binary32, scaled per 16-block.
+template <typename P>
+__device__ void rank1_rows(const P& p, int64_t n0, int64_t n1, const uint8_t* s_codes, const uint8_t* s_scales,
+                           float s_mu) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float s = __fmul_rn(s_mu, __ldg(p.w_ts));
+  const int64_t nch = p.C / 32, nb = p.C / 16;
+  for (int64_t n = n0 + warp; n < n1; n += 8) {
+    float acc = 0.f;
+    const uint8_t* wrow = p.w_codes + n * p.w_ld;
+    for (int64_t j = lane; j < nch + (nb & 1); j += 32) {
+      const bool two = 2 * j + 1 < nb;
+      const uint4 wc = two ? __ldg(reinterpret_cast<const uint4*>(wrow + 16 * j))
+                           : make_uint4(*reinterpret_cast<const uint32_t*>(wrow + 16 * j),
+                                        *reinterpret_cast<const uint32_t*>(wrow + 16 * j + 4), 0u, 0u);
+      const uint4 mc = two ? *reinterpret_cast<const uint4*>(s_codes + 16 * j)
+                           : make_uint4(*reinterpret_cast<const uint32_t*>(s_codes + 16 * j),
+                                        *reinterpret_cast<const uint32_t*>(s_codes + 16 * j + 4), 0u, 0u);
+      const float d0 = dot16_codes(make_uint2(wc.x, wc.y), make_uint2(mc.x, mc.y));
+      acc = fmaf(d0, __fmul_rn(e4m3_value(p.w_scales[scale_offset(n, 2 * j, p.w_kc)]), e4m3_value(s_scales[2 * j])),
+                 acc);
+      if (two) {
+        const float d1 = dot16_codes(make_uint2(wc.z, wc.w), make_uint2(mc.z, mc.w));
+        acc = fmaf(d1, __fmul_rn(e4m3_value(p.w_scales[scale_offset(n, 2 * j + 1, p.w_kc)]),
+                                 e4m3_value(s_scales[2 * j + 1])), acc);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) p.r_out[n] = acc * s;
   }
 }
 
@@ -461,6 +537,16 @@ struct QuantParams {
   float* col_ts;
   int64_t col_ld, col_kc;
   int tiles_r, tiles_c;
+  // CTAs [0, mean_ctas) quantize the mean and compute the rank-one row; the
+  // rest quantize tiles
+  int mean_ctas;
+  // optional rank-one row (split only): r[N] = deq(mu_q) deq(W)^T, with W an
+  // NVFP4 [N, C] tensor blocked along C (the blocking of the mean)
+  const uint8_t* w_codes;
+  const uint8_t* w_scales;
+  const float* w_ts;
+  int64_t w_rows, w_ld, w_kc;
+  float* r_out;
 };
 
 constexpr int kQTile = 128;
@@ -675,6 +761,8 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const int tid = threadIdx.x, warp = tid >> 5;
   const int ntiles = p.tiles_r * p.tiles_c;
   const bool split = p.mu != nullptr;
+  const bool mean_cta = (int)blockIdx.x < p.mean_ctas;
+  const int tcta = (int)blockIdx.x - p.mean_ctas, ntcta = (int)gridDim.x - p.mean_ctas;  // tile CTA index, count
   const bool rows_on = AMAX_ONLY || p.row_codes != nullptr;
   const bool cols_on = AMAX_ONLY || p.col_codes != nullptr;
 
@@ -689,8 +777,9 @@ __global__ void __launch_bounds__(kQThreads, 2)
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmX);
     // the input was written before the previous kernel started: fetch while it finishes
-    for (int b = 0; b < kQBufs; ++b)
-      if ((int)(blockIdx.x + b * gridDim.x) < ntiles) issue(blockIdx.x + b * gridDim.x, b);
+    if (!mean_cta)
+      for (int b = 0; b < kQBufs; ++b)
+        if (tcta + b * ntcta < ntiles) issue(tcta + b * ntcta, b);
   }
   ptx::pdl_wait_and_release();
 
@@ -710,11 +799,20 @@ __global__ void __launch_bounds__(kQThreads, 2)
   }
   const float den_row = __fmul_rn(6.0f, s_row), den_col = __fmul_rn(6.0f, s_col);
   float amax_row = 0.f, amax_col = 0.f;
-  if (!AMAX_ONLY && split && blockIdx.x == gridDim.x - 1)
-    quantize_mean(p.mu, p.C, p.hadamard != 0, p.mu_codes, p.mu_scales, p.mu_ts, p.mu_hat, p.mu_kc, red);
+  if (!AMAX_ONLY && split && mean_cta) {
+    // the mean as NVFP4 (CTA 0 writes it out) and this CTA's share of the rank-one row
+    uint8_t* s_codes = sm;                        // tile buffers are unused in a mean CTA
+    uint8_t* s_scales = sm + kQOffMu - kQBufs * kQTileBytes / 4;
+    const float s_mu = quantize_mean(p, blockIdx.x == 0, s_codes, s_scales, red);
+    if (p.r_out != nullptr) {
+      const int64_t per = (p.w_rows + p.mean_ctas - 1) / p.mean_ctas;
+      const int64_t n0 = (int64_t)blockIdx.x * per;
+      rank1_rows(p, n0, min(p.w_rows, n0 + per), s_codes, s_scales, s_mu);
+    }
+  }
 
   int i = 0;
-  for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++i) {
+  for (int tile = mean_cta ? ntiles : tcta; tile < ntiles; tile += ntcta, ++i) {
     const int b = i % kQBufs;
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     const int64_t r0 = (int64_t)tr * kQTile, c0 = (int64_t)tc * kQTile;
@@ -733,7 +831,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
       quant_cols<AMAX_ONLY>(p, buf, mub, r0, c0, split, den_col, s_col > 0.f, inv_s + 128, cs, amax_col);
     }
     __syncthreads();  // the tile buffer and the scale staging are complete
-    if (tid == 0 && tile + kQBufs * (int)gridDim.x < ntiles) issue(tile + kQBufs * gridDim.x, b);
+    if (tid == 0 && tile + kQBufs * ntcta < ntiles) issue(tile + kQBufs * ntcta, b);
     if (!AMAX_ONLY && p.col_codes != nullptr && tid < 64) {
       // column-layout scale atoms: row chunk tc, chunks 2*tr and 2*tr + 1
       const int64_t kc = 2 * (int64_t)tr + (tid >> 5);
