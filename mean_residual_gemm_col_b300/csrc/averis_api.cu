@@ -247,7 +247,7 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   }
   if (out_row == nullptr && out_col == nullptr) qp.tiles_r = 0;  // mean only
   // mean CTAs: one for the mean alone, more when they also compute the
-  // rank-one row (about 256 K weights each, at most 32)
+  // rank-one row (about 128 K weights each, at most 64)
   qp.mean_ctas = 0;
   if (split) {
     qp.mean_ctas = 1;
@@ -259,7 +259,7 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
       qp.w_ld = averis_nvfp4_ld(C);
       qp.w_kc = cdiv(C, 64);
       qp.r_out = r_out;
-      qp.mean_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(32, cdiv(r_w->rows * C, (int64_t)1 << 18)));
+      qp.mean_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(64, cdiv(r_w->rows * C, (int64_t)1 << 17)));
     }
   }
   const int ntiles = qp.tiles_r * qp.tiles_c;
@@ -292,8 +292,11 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t in
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// early_start: the kernel launched just before this GEMM produced none of its
+// inputs (see GemmParams::early_start).
 averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const float* col_add, const float* row_vec,
-                        const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s) {
+                        const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s,
+                        bool early_start = false) {
   if (a == nullptr || b == nullptr || out == nullptr) return AVERIS_ERR_INVALID_ARG;
   const int64_t M = a->rows, N = b->rows, K = a->cols;
   // K may be ragged (the token axis of dW): codes and scales are zero-padded to 64
@@ -337,6 +340,7 @@ averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const floa
   p.col_vec = col_vec;
   p.outer = outer;
   p.err = dev->err_word;
+  p.early_start = early_start ? 1 : 0;
   const int64_t ntiles = cdiv(M, Cfg::BM) * cdiv(N, BN);
   const int grid = (int)std::min<int64_t>(ntiles, dev->sms);
   cudaError_t e = bf16 ? launch_pdl(gemm_nvfp4_kernel<true>, dim3(grid), dim3(192), Cfg::SMEM, s, ta, tb, td, p)
@@ -434,8 +438,10 @@ averis_status linear_bwd_impl(const void* d, int64_t l, int64_t m, int64_t n, co
   if (r != AVERIS_OK) return r;
   if ((r = gemm_impl(&d_row, w_n, split ? r_d : nullptr, nullptr, nullptr, 0.f, dx, m, flags, s)) != AVERIS_OK)
     return r;
+  // dW reads the forward state and D's quantized column layout, not dX: it
+  // starts while the input-gradient GEMM drains
   return gemm_impl(&st->x_col, &d_col, nullptr, split ? st->mu_hat : nullptr, split ? mu_hat : nullptr, (float)l, dw,
-                   n, flags & ~AVERIS_OUT_BF16, s);
+                   n, flags & ~AVERIS_OUT_BF16, s, /*early_start=*/true);
 }
 
 }  // namespace

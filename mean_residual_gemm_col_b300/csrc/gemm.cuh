@@ -54,6 +54,11 @@ struct GemmParams {
   const float* col_vec;  // [N] or null
   float outer;
   int* err;
+  // 1: none of this GEMM's inputs comes from the kernel launched just before
+  // it (the library issues it right after an independent GEMM): start at
+  // once, and wait for that kernel only before exiting, so that this
+  // kernel's completion still implies the previous one's.
+  int early_start;
 };
 
 
@@ -142,7 +147,10 @@ __global__ void __launch_bounds__(192, 1)
   ptx::tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // operands, scales and epilogue vectors may come from the previous kernel
-  ptx::pdl_wait_and_release();
+  if (p.early_start)
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  else
+    ptx::pdl_wait_and_release();
 
   const int num_m = (p.M + Cfg::BM - 1) / Cfg::BM;
   const int num_n = (p.N + BN - 1) / BN;
@@ -347,6 +355,7 @@ done:
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, Cfg::TMEM_COLS);
   }
+  if (p.early_start) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace averis

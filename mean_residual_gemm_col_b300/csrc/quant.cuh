@@ -456,59 +456,85 @@ __device__ __forceinline__ void e2m1x8_to_h2(uint32_t w, uint32_t (&h)[4]) {
       : "r"(w));
 }
 
-// Sum of the 16 products of two NVFP4 code blocks (two words each).  Each
-// product of E2M1 values is a multiple of 1/4 of magnitude <= 36, and each
-// f16 half accumulates 8 of them (<= 288, 1152 quarter units < 2^11): every
-// step is exact in f16, and the final binary32 sum is exact too.
-__device__ __forceinline__ float dot16_codes(uint2 a, uint2 b) {
-  uint32_t ha[4], hb[4];
+// Dot product of one 16-element block of codes (two words, already unpacked
+// into f16 pairs for the mean) with the same block of another code row.
+// Each product of E2M1 values is a multiple of 1/4 of magnitude <= 36, and
+// each f16 half accumulates 8 of them (<= 288, 1152 quarter units < 2^11):
+// every step is exact in f16, and the final binary32 sum is exact too.
+__device__ __forceinline__ float dot16_h2(const uint32_t (&mh)[8], uint32_t w0, uint32_t w1) {
+  uint32_t wh[4];
   __half2 acc = __float2half2_rn(0.f);
-  e2m1x8_to_h2(a.x, ha);
-  e2m1x8_to_h2(b.x, hb);
+  e2m1x8_to_h2(w0, wh);
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    acc = __hfma2(*reinterpret_cast<__half2*>(&ha[k]), *reinterpret_cast<__half2*>(&hb[k]), acc);
-  e2m1x8_to_h2(a.y, ha);
-  e2m1x8_to_h2(b.y, hb);
+    acc = __hfma2(*reinterpret_cast<const __half2*>(&mh[k]), *reinterpret_cast<__half2*>(&wh[k]), acc);
+  e2m1x8_to_h2(w1, wh);
 #pragma unroll
   for (int k = 0; k < 4; ++k)
-    acc = __hfma2(*reinterpret_cast<__half2*>(&ha[k]), *reinterpret_cast<__half2*>(&hb[k]), acc);
+    acc = __hfma2(*reinterpret_cast<const __half2*>(&mh[4 + k]), *reinterpret_cast<__half2*>(&wh[k]), acc);
   const float2 f = __half22float2(acc);
   return f.x + f.y;
 }
 
 // Rank-one row r[n] = s_mu s_w sum_k deq(mu)_k deq(W)_{n,k} for rows
-// [n0, n1) of W, with the NVFP4 mean in SMEM.  Warp per row, lanes over
-// 32-element chunks; block products in binary32, scaled per 16-block.
+// [n0, n1) of W, with the NVFP4 mean in SMEM.  A warp handles 4 rows at a
+// time (all their loads in flight together), lanes over 32-element chunks;
+// block products in f16 (exact), scaled per 16-block in binary32.
 template <typename P>
 __device__ void rank1_rows(const P& p, int64_t n0, int64_t n1, const uint8_t* s_codes, const uint8_t* s_scales,
                            float s_mu) {
+  constexpr int RW = 4;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float s = __fmul_rn(s_mu, __ldg(p.w_ts));
-  const int64_t nch = p.C / 32, nb = p.C / 16;
-  for (int64_t n = n0 + warp; n < n1; n += 8) {
-    float acc = 0.f;
-    const uint8_t* wrow = p.w_codes + n * p.w_ld;
-    for (int64_t j = lane; j < nch + (nb & 1); j += 32) {
+  const int64_t nb = p.C / 16;
+  const int64_t nch = (nb + 1) / 2;  // 32-element chunks (the last may hold one block)
+  for (int64_t nr = n0 + RW * warp; nr < n1; nr += RW * 8) {
+    float acc[RW];
+#pragma unroll
+    for (int i = 0; i < RW; ++i) acc[i] = 0.f;
+    for (int64_t j = lane; j < nch; j += 32) {
       const bool two = 2 * j + 1 < nb;
-      const uint4 wc = two ? __ldg(reinterpret_cast<const uint4*>(wrow + 16 * j))
-                           : make_uint4(*reinterpret_cast<const uint32_t*>(wrow + 16 * j),
-                                        *reinterpret_cast<const uint32_t*>(wrow + 16 * j + 4), 0u, 0u);
+      uint4 wc[RW];
+      uint32_t wsc[RW];
+#pragma unroll
+      for (int i = 0; i < RW; ++i) {
+        const int64_t n = min(nr + i, n1 - 1);
+        const uint8_t* wrow = p.w_codes + n * p.w_ld + 16 * j;
+        wc[i] = two ? __ldg(reinterpret_cast<const uint4*>(wrow))
+                    : make_uint4(__ldg(reinterpret_cast<const uint32_t*>(wrow)),
+                                 __ldg(reinterpret_cast<const uint32_t*>(wrow + 4)), 0u, 0u);
+        // blocks 2j, 2j+1 of a row sit in adjacent bytes of one scale atom
+        const uint8_t* sp = p.w_scales + scale_offset(n, 2 * j, p.w_kc);
+        wsc[i] = two ? __ldg(reinterpret_cast<const uint16_t*>(sp)) : __ldg(sp);
+      }
       const uint4 mc = two ? *reinterpret_cast<const uint4*>(s_codes + 16 * j)
                            : make_uint4(*reinterpret_cast<const uint32_t*>(s_codes + 16 * j),
                                         *reinterpret_cast<const uint32_t*>(s_codes + 16 * j + 4), 0u, 0u);
-      const float d0 = dot16_codes(make_uint2(wc.x, wc.y), make_uint2(mc.x, mc.y));
-      acc = fmaf(d0, __fmul_rn(e4m3_value(p.w_scales[scale_offset(n, 2 * j, p.w_kc)]), e4m3_value(s_scales[2 * j])),
-                 acc);
-      if (two) {
-        const float d1 = dot16_codes(make_uint2(wc.z, wc.w), make_uint2(mc.z, mc.w));
-        acc = fmaf(d1, __fmul_rn(e4m3_value(p.w_scales[scale_offset(n, 2 * j + 1, p.w_kc)]),
-                                 e4m3_value(s_scales[2 * j + 1])), acc);
+      uint32_t m0[8], m1[8];
+      e2m1x8_to_h2(mc.x, *reinterpret_cast<uint32_t(*)[4]>(&m0[0]));
+      e2m1x8_to_h2(mc.y, *reinterpret_cast<uint32_t(*)[4]>(&m0[4]));
+      e2m1x8_to_h2(mc.z, *reinterpret_cast<uint32_t(*)[4]>(&m1[0]));
+      e2m1x8_to_h2(mc.w, *reinterpret_cast<uint32_t(*)[4]>(&m1[4]));
+      const float ms0 = e4m3_value(s_scales[2 * j]);
+      const float ms1 = two ? e4m3_value(s_scales[2 * j + 1]) : 0.f;
+#pragma unroll
+      for (int i = 0; i < RW; ++i) {
+        acc[i] = fmaf(dot16_h2(m0, wc[i].x, wc[i].y), __fmul_rn(e4m3_value(wsc[i] & 0xFFu), ms0), acc[i]);
+        if (two) acc[i] = fmaf(dot16_h2(m1, wc[i].z, wc[i].w), __fmul_rn(e4m3_value(wsc[i] >> 8), ms1), acc[i]);
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) p.r_out[n] = acc * s;
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int i = 0; i < RW; ++i) acc[i] += __shfl_xor_sync(0xffffffffu, acc[i], o);
+    }
+    if (lane < RW && nr + lane < n1) {
+      float v = acc[0];
+#pragma unroll
+      for (int i = 1; i < RW; ++i)
+        if (lane == i) v = acc[i];
+      p.r_out[nr + lane] = v * s;
+    }
   }
 }
 
