@@ -206,11 +206,12 @@ def run_step(layers, mode):
 
 
 def launches_per_step(mode):
+    """Kernels one step enqueues: per linear, weight quantize (stats, quantize),
+    forward (stats, quantize, GEMM), backward (stats, quantize, 2 GEMMs); the
+    Hadamard modes add the rotated-maximum pass to each of the three quantizes."""
     had = mode in ("averis_h16", "nvfp4_h16")
-    split = mode in ("averis", "averis_h16")
-    q = 4 if had else 3                       # stats, finalize, (amax), quantize
-    per = q + (q + (1 if split else 0) + 1) + (q + (1 if split else 0) + 2)
-    return per * len(LINEARS)
+    q = 3 if had else 2
+    return (q + (q + 1) + (q + 2)) * len(LINEARS)
 
 
 def kernel_groups(layers):
@@ -290,7 +291,7 @@ def run_ours(args, rank, ws):
     for ly in layers:
         ly.xq = capi.averis_quantize(ly.x, capi.AVERIS_MEAN_SPLIT)
         ly.dq = capi.averis_quantize(ly.d, capi.AVERIS_MEAN_SPLIT)
-    modes = ["averis", "nvfp4", "averis_h16"]
+    modes = ["averis", "nvfp4", "averis_h16", "nvfp4_h16"]
     for mode in modes:       # eager warm-up: kernel attributes, workspaces, first-call setup
         run_step(layers, mode)
     torch.cuda.synchronize()
@@ -323,10 +324,11 @@ def run_ours(args, rank, ws):
 
     # ---- comparison modes and per-kernel timing (same inputs, same launches)
     for _ in range(args.warmup):
-        graphs["nvfp4"].replay()
-        graphs["averis_h16"].replay()
+        for m in ("nvfp4", "averis_h16", "nvfp4_h16"):
+            graphs[m].replay()
     ms_van = max_over_ranks(time_graph(graphs["nvfp4"], args.steps, stream), ws)
     ms_had = max_over_ranks(time_graph(graphs["averis_h16"], args.steps, stream), ws)
+    ms_vhad = max_over_ranks(time_graph(graphs["nvfp4_h16"], args.steps, stream), ws)
     kern = {}
     for k, g in ggraphs.items():
         g.replay()
@@ -407,8 +409,11 @@ def run_ours(args, rank, ws):
         "fp4_peak_sustained_tflops": round(fp4_sus, 1),
         "overhead_vs_vanilla": round((ms - ms_van) / ms_van, 4),
         "overhead_h16_vs_vanilla": round((ms_had - ms_van) / ms_van, 4),
+        "overhead_nvfp4_h16_vs_vanilla": round((ms_vhad - ms_van) / ms_van, 4),
+        "averis_overhead_over_hadamard_overhead": round((ms - ms_van) / max(ms_vhad - ms_van, 1e-9), 4),
         "ms_per_step_vanilla": round(ms_van, 4),
         "ms_per_step_averis_h16": round(ms_had, 4),
+        "ms_per_step_nvfp4_h16": round(ms_vhad, 4),
         "roofline": {k: (round(v, 4) if isinstance(v, float) else v) for k, v in roof.items()},
         "kernels_ms_per_step": {k: round(v, 4) for k, v in kern.items()},
         "quantize_pass": {"avg_ms": round(q_ms, 4), "algorithmic_gbs": round(q_bytes / (q_ms * 1e-3) / 1e9, 1),
@@ -420,9 +425,116 @@ def run_ours(args, rank, ws):
         "clocks": clocks,
         "wall_s_timed": round(wall, 4),
     }
+    if not args.no_extras:
+        del graphs, ggraphs
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        line["quantize_sweep"] = quantize_sweep(peaks)
+        line["preprocess_vs_hadamard"] = preprocess_comparison()
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
+
+
+# ------------------------------------------------ quantize-only measurements --
+
+def _time_each(fn, iters, flush, stream):
+    """Median device time of ``fn`` (ms), L2 flushed before each timed call."""
+    import torch
+
+    ts = []
+    for _ in range(iters):
+        flush.zero_()
+        s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        torch.cuda.synchronize()
+        ts.append(s.elapsed_time(e))
+    return statistics.median(ts)
+
+
+def _quantizer(x, flags):
+    """A closure that runs the fused quantize pass on x with preallocated outputs."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    lib = capi.load()
+    R, C = x.shape
+    dev = x.device
+    row = capi.NVFP4Tensor.empty(R, C, dev)
+    col = capi.NVFP4Tensor.empty(C, R, dev)
+    mu = torch.zeros(C, device=dev)
+    muh = torch.zeros(C, device=dev)
+    muq = capi.NVFP4Tensor.empty(1, C, dev)
+    ws = capi.workspace(lib.averis_quantize_workspace_bytes(R, C, flags), dev, "sweep")
+    rs, cs, ms = row.struct(), col.struct(), muq.struct()
+    st = capi._stream(dev)
+
+    def run():
+        capi._check(lib.averis_quantize(capi._ptr(x), R, C, flags, capi._ptr(mu), ctypes.byref(ms), capi._ptr(muh),
+                                        ctypes.byref(rs), ctypes.byref(cs), capi._ptr(ws), ws.numel(), st),
+                    "averis_quantize")
+    return run, (row, col, mu, muh, muq, ws)
+
+
+def quantize_sweep(peaks, iters=5):
+    """The quantize-only sweep: fused mean-split NVFP4 of an l x m bf16 activation
+    into both layouts, l in {4096, 16384, 65536} x m in {1024, 2048, 4096, 8192}.
+    Algorithmic bytes per element: 2 (bf16 read) + 2 x (0.5 + 1/16) (both layouts)."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    out = []
+    for l in workloads.QUANT_SWEEP_L:
+        for m in workloads.QUANT_SWEEP_M:
+            x = workloads.torch_activation(l * 10 + m, l, m, spike=50.0, device=dev)
+            run, keep = _quantizer(x, capi.AVERIS_MEAN_SPLIT)
+            run()
+            torch.cuda.synchronize()
+            ms = _time_each(run, iters, flush, stream)
+            gbs = 3.125 * l * m / (ms * 1e-3) / 1e9
+            out.append({"l": l, "m": m, "us": round(ms * 1e3, 1), "algorithmic_gbs": round(gbs, 1),
+                        "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)})
+            del x, run, keep
+    torch.cuda.empty_cache()
+    return out
+
+
+def preprocess_comparison(iters=3):
+    """Quantize-pass latency of vanilla NVFP4, Averis (mean split) and NVFP4 with the
+    16x16 Hadamard rotation on activations of 512 x 2048 tokens, d = 4096 / 8192
+    (the shapes of the pages' preprocessing-latency table).  The Averis and
+    Hadamard preprocessing costs are the differences to the vanilla pass."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    res = []
+    for d in (4096, 8192):
+        l = 512 * 2048
+        x = workloads.torch_activation(d, l, d, spike=50.0, device=dev)
+        t = {}
+        for name, flags in (("vanilla", 0), ("averis", capi.AVERIS_MEAN_SPLIT), ("hadamard", capi.AVERIS_HADAMARD16)):
+            run, keep = _quantizer(x, flags)
+            run()
+            torch.cuda.synchronize()
+            t[name] = _time_each(run, iters, flush, stream)
+            del run, keep
+            torch.cuda.empty_cache()
+        ov_a, ov_h = t["averis"] - t["vanilla"], t["hadamard"] - t["vanilla"]
+        res.append({"tokens": l, "d": d, "ms_vanilla": round(t["vanilla"], 3), "ms_averis": round(t["averis"], 3),
+                    "ms_hadamard": round(t["hadamard"], 3), "averis_extra_ms": round(ov_a, 3),
+                    "hadamard_extra_ms": round(ov_h, 3),
+                    "hadamard_extra_over_averis_extra": round(ov_h / ov_a, 2) if ov_a > 0 else None})
+        del x
+        torch.cuda.empty_cache()
+    return res
 
 
 # --------------------------------------------------------- CPU baseline ----
@@ -484,10 +596,11 @@ def run_reference(args, rank, ws):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the quantize sweep and the preprocessing table")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     args = ap.parse_args()
     if args.warmup < 3:

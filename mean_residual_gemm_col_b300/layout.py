@@ -25,10 +25,10 @@ def scale_bytes(rows: int, cols: int) -> int:
     return 512 * cdiv(rows, 128) * cdiv(cols, 64)
 
 
-def scale_offsets(rows: int, cols: int) -> np.ndarray:
-    """int64 [rows, ceil(cols/16)]: byte offset of each block scale."""
+def scale_offsets(rows: int, cols: int, row_idx=None) -> np.ndarray:
+    """int64 [rows, ceil(cols/16)]: byte offset of each block scale (only the rows ``row_idx`` if given)."""
     kc = cdiv(cols, 64)
-    r = np.arange(rows, dtype=np.int64)[:, None]
+    r = (np.arange(rows, dtype=np.int64) if row_idx is None else np.asarray(row_idx, dtype=np.int64))[:, None]
     k = np.arange(cdiv(cols, 16), dtype=np.int64)[None, :]
     return ((r // 128) * kc + k // 4) * 512 + 16 * (r % 32) + 4 * ((r % 128) // 32) + (k % 4)
 
