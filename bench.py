@@ -44,6 +44,22 @@ FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustain
 CPU_SAMPLE_TOKENS = 256
 
 
+# DRAM bytes (read + write) per GEMM launch of this step, averaged over the 12
+# GEMM launches of one ncu capture (profiles/dram_traffic_qwen3_step.md), valid
+# only for the GEMM source it was taken on.
+GEMM_TRAFFIC = {"ad947d59d2fa3f73": 245.8e6 / 12}
+
+
+def gemm_traffic_per_launch():
+    import hashlib
+
+    h = hashlib.sha256()
+    for f in ("gemm.cuh", "ptx.cuh"):
+        with open(os.path.join(ROOT, "mean_residual_gemm_col_b300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return GEMM_TRAFFIC.get(h.hexdigest()[:16])
+
+
 def flops_per_step(l=L):
     return sum(6.0 * l * m * n + 5.0 * m * n for _, m, n in LINEARS)
 
@@ -384,7 +400,7 @@ def run_ours(args, rank, ws):
                 "unit": "GB/s"}
         psrc = f"{src} hbm_gbs"
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = None
+    roof["traffic"] = gemm_traffic_per_launch()
     roof["kernel"] = "gemm_nvfp4_kernel, mean of the 12 GEMM launches of a step"
     roof["peak_source"] = psrc
     line = {
