@@ -176,19 +176,25 @@ class ClockSampler:
 class Layer:
     """One linear's inputs, outputs and every intermediate buffer, preallocated."""
 
-    def __init__(self, name, m, n, seed, device):
+    def __init__(self, name, m, n, seed, device, l=L, share=None):
         import torch
         from mean_residual_gemm_col_b300 import capi
 
         self.name, self.m, self.n = name, m, n
-        self.x, self.w, self.d = workloads.torch_linear_case(seed, L, m, n, spike=workloads.QWEN3_SPIKE,
-                                                             device=device)
+        if share is None:
+            self.x, self.w, self.d = workloads.torch_linear_case(seed, l, m, n, spike=workloads.QWEN3_SPIKE,
+                                                                 device=device)
+            self.state = capi.FwdState.empty(l, m, device)
+            self.y = torch.empty(l, n, dtype=torch.bfloat16, device=device)
+            self.dx = torch.empty(l, m, dtype=torch.bfloat16, device=device)
+            self.dw = torch.empty(m, n, dtype=torch.float32, device=device)
+        else:
+            # another layer of a stack: its own weights, the shared activations and buffers
+            _, self.w, _ = workloads.torch_linear_case(seed, 64, m, n, device=device)
+            self.x, self.d, self.state, self.y, self.dx, self.dw = (share.x, share.d, share.state, share.y,
+                                                                   share.dx, share.dw)
         self.w_n = capi.NVFP4Tensor.empty(m, n, device)
         self.w_m = capi.NVFP4Tensor.empty(n, m, device)
-        self.state = capi.FwdState.empty(L, m, device)
-        self.y = torch.empty(L, n, dtype=torch.bfloat16, device=device)
-        self.dx = torch.empty(L, m, dtype=torch.bfloat16, device=device)
-        self.dw = torch.empty(m, n, dtype=torch.float32, device=device)
         self.xq = None   # standalone quantized X / D (same kernels) for the per-kernel timing
         self.dq = None
 
@@ -204,14 +210,41 @@ def quant_weight_into(ly, flags):
                 "averis_quantize_weight")
 
 
+_SIDE = {}
+
+
+def side_stream(device):
+    import torch
+
+    if device not in _SIDE:
+        _SIDE[device] = torch.cuda.Stream(device)
+    return _SIDE[device]
+
+
 def run_step(layers, mode):
-    """Enqueue one fwd+bwd step of every layer on the current stream."""
+    """Enqueue one fwd+bwd step of every layer.
+
+    The weights do not depend on the activations, so their quantization runs
+    on a side stream (joined per layer by an event) while the main stream
+    runs the layers' forward and backward passes in order.
+    """
+    import torch
     from mean_residual_gemm_col_b300 import capi
 
     split = mode in ("averis", "averis_h16")
     hf = capi.AVERIS_HADAMARD16 if mode in ("averis_h16", "nvfp4_h16") else 0
-    for ly in layers:
-        quant_weight_into(ly, hf)
+    main = torch.cuda.current_stream()
+    side = side_stream(main.device)
+    side.wait_stream(main)
+    ready = []
+    with torch.cuda.stream(side):
+        for ly in layers:
+            quant_weight_into(ly, hf)
+            ev = torch.cuda.Event()
+            ev.record(side)
+            ready.append(ev)
+    for ly, ev in zip(layers, ready):
+        main.wait_event(ev)
         if split:
             capi.averis_linear_fwd(ly.x, ly.w_m, capi.AVERIS_MEAN_SPLIT | hf, out_bf16=True, state=ly.state, y=ly.y)
             capi.averis_linear_bwd(ly.d, ly.state, ly.w_n, capi.AVERIS_MEAN_SPLIT | hf, out_bf16=True, dx=ly.dx,
@@ -447,6 +480,8 @@ def run_ours(args, rank, ws):
         torch.cuda.empty_cache()
         line["quantize_sweep"] = quantize_sweep(peaks)
         line["preprocess_vs_hadamard"] = preprocess_comparison()
+        line["stack_28_layers"] = stack_comparison()
+        line["quant_error_qkv"] = quant_error_diagnostic(layers[0])
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
@@ -551,6 +586,78 @@ def preprocess_comparison(iters=3):
         del x
         torch.cuda.empty_cache()
     return res
+
+
+def _dequant_gpu(t):
+    """float32 [rows, cols] value of an NVFP4 tensor of the library (measurement only)."""
+    import torch
+    from mean_residual_gemm_col_b300 import layout
+
+    dev = t.codes.device
+    e2m1 = torch.tensor([0, .5, 1, 1.5, 2, 3, 4, 6, -0., -.5, -1, -1.5, -2, -3, -4, -6], device=dev)
+    c = t.codes.long()
+    vals = torch.stack([e2m1[c & 15], e2m1[c >> 4]], dim=-1).reshape(t.rows, -1)[:, : t.cols]
+    off = torch.from_numpy(layout.scale_offsets(t.rows, t.cols)).to(dev)
+    sc = t.scales.view(torch.float8_e4m3fn).float()[off]
+    return (vals.reshape(t.rows, -1, 16) * sc[:, :, None]).reshape(t.rows, -1)[:, : t.cols] * t.tensor_scale
+
+
+def quant_error_diagnostic(layer):
+    """Relative NVFP4 error ||deq(Q(T)) - T|| / ||T|| of one linear's activation X and
+    output gradient D, quantized directly (vanilla) and as mean + residual (Averis:
+    deq(Q(T - 1 mu)) + 1 deq(Q(mu)))."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    res = {}
+    for name, t in (("X", layer.x), ("D", layer.d)):
+        ref = t.float()
+        van = capi.averis_quantize(t, 0, want_col=False)
+        av = capi.averis_quantize(t, capi.AVERIS_MEAN_SPLIT, want_col=False)
+        e_van = _dequant_gpu(van["row"]) - ref
+        e_av = _dequant_gpu(av["row"]) + av["mu_hat"][None, :] - ref
+        nrm = torch.linalg.vector_norm(ref)
+        res[name] = {"vanilla": round(float(torch.linalg.vector_norm(e_van) / nrm), 5),
+                     "averis": round(float(torch.linalg.vector_norm(e_av) / nrm), 5)}
+        del ref, van, av, e_van, e_av
+    return res
+
+
+def stack_comparison(steps=3, warmup=2):
+    """28-layer stack of the Qwen3-0.6B linears at l = 16384 (b = 8, s = 2048),
+    fwd + bwd, in three modes: vanilla NVFP4, Averis, Averis + 16x16 Hadamard on
+    the residual.  Every layer has its own weights (seed = layer); the planted-mean
+    activations and output gradients are shared by all layers."""
+    import torch
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    lst = workloads.STACK_L
+    base = [Layer(name, m, n, seed=5000 + i, device=dev, l=lst) for i, (name, m, n) in enumerate(LINEARS)]
+    stack = []
+    for layer in range(workloads.STACK_LAYERS):
+        for i, (name, m, n) in enumerate(LINEARS):
+            stack.append(Layer(name, m, n, seed=layer, device=dev, l=lst, share=base[i]))
+    flops = workloads.STACK_LAYERS * flops_per_step(lst)
+    out = {"layers": workloads.STACK_LAYERS, "l": lst, "tflop_per_step": round(flops / 1e12, 3)}
+    stream = torch.cuda.current_stream()
+    ms = {}
+    for mode in ("nvfp4", "averis", "averis_h16"):
+        run_step(stack, mode)
+        torch.cuda.synchronize()
+        g = capture(lambda mode=mode: run_step(stack, mode))
+        for _ in range(warmup):
+            g.replay()
+        ms[mode] = time_graph(g, steps, stream)
+        del g
+    for mode, t in ms.items():
+        out[f"ms_{mode}"] = round(t, 3)
+        out[f"tflops_{mode}"] = round(flops / (t * 1e-3) / 1e12, 1)
+    out["overhead_averis"] = round((ms["averis"] - ms["nvfp4"]) / ms["nvfp4"], 4)
+    out["overhead_averis_h16"] = round((ms["averis_h16"] - ms["nvfp4"]) / ms["nvfp4"], 4)
+    del stack, base
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 # --------------------------------------------------------- CPU baseline ----
