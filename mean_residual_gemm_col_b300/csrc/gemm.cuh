@@ -78,7 +78,8 @@ struct GemmCfg {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_BAR = OFF_EPI + EPI_BYTES;
+  static constexpr int OFF_VEC = OFF_EPI + EPI_BYTES;  // [2 tile parities][col_add, col_vec][BN] floats
+  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BN * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // + alignment slack
   // TMEM columns: the accumulator, then per stage 16 SFA columns + BN/8 SFB columns
   static constexpr int SF_BASE = BN;
@@ -94,17 +95,26 @@ struct GemmCfg {
 };
 
 // Epilogue value of one accumulator column chunk: alpha * acc + col_add + rterm * col_vec.
-// `cadd`/`cvec` hold the vector entry of column (chunk + lane) in each lane.
-__device__ __forceinline__ void epi_math(float (&f)[32], const uint32_t (&v)[32], float alpha, bool has_add,
-                                         float cadd, bool has_outer, float rterm, float cvec) {
+// `cadd`/`cvec` point at the chunk's 32 vector entries in SMEM (broadcast reads).
+__device__ __forceinline__ void epi_math(float (&f)[32], const float (&acc)[32], bool has_add, const float* cadd,
+                                         bool has_outer, float rterm, const float* cvec) {
 #pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    float x = alpha * __uint_as_float(v[j]);
-    if (has_add) x += __shfl_sync(0xffffffffu, cadd, j);
-    if (has_outer) x = fmaf(rterm, __shfl_sync(0xffffffffu, cvec, j), x);
-    f[j] = x;
+  for (int j4 = 0; j4 < 8; ++j4) {
+    const float4 a4 = has_add ? *reinterpret_cast<const float4*>(cadd + 4 * j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float4 v4 = has_outer ? *reinterpret_cast<const float4*>(cvec + 4 * j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    const float a[4] = {a4.x, a4.y, a4.z, a4.w}, v[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      float x = acc[4 * j4 + k];
+      if (has_add) x += a[k];
+      if (has_outer) x = fmaf(rterm, v[k], x);
+      f[4 * j4 + k] = x;
+    }
   }
 }
+
+// Named barrier of the four epilogue warps (ids 1 and up are free for this).
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 template <bool BF16_OUT>
 __global__ void __launch_bounds__(192, 1)
@@ -156,17 +166,25 @@ __global__ void __launch_bounds__(192, 1)
   const int num_n = (p.N + BN - 1) / BN;
   const int ntiles = num_m * num_n;
   const int nkt = (p.kc + 3) / 4;
+  // output tile `tile` -> (mt, nt), M fastest; every tile runs over all K tiles
+  auto decode = [&](int tile, int& mt, int& nt, int& kt0, int& kt1) {
+    mt = tile % num_m;
+    nt = tile / num_m;
+    kt0 = 0;
+    kt1 = nkt;
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-        const int mt = tile % num_m, nt = tile / num_m;
+        int mt, nt, kt0, kt1;
+        decode(tile, mt, nt, kt0, kt1);
         int nsfb = 0;
 #pragma unroll
         for (int h = 0; h < BN / 128; ++h) nsfb += (nt * (BN / 128) + h) < p.rb_b ? 1 : 0;
-        for (int kt = 0; kt < nkt; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
           if (!ptx::mbar_wait(&empty[stage], phase ^ 1u, kWaitLimit)) {
             atomicExch(p.err, kErrProducer);
             goto done;
@@ -199,13 +217,15 @@ __global__ void __launch_bounds__(192, 1)
       int it = 0;
       bool issued = false;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
+        int mt, nt, kt0, kt1;
+        decode(tile, mt, nt, kt0, kt1);
         if (!ptx::mbar_wait(tempty, (it & 1) ^ 1u, kWaitLimit)) {
           atomicExch(p.err, kErrMma);
           break;
         }
         ptx::tc_fence_after();
         bool ok = true;
-        for (int kt = 0; kt < nkt; ++kt) {
+        for (int kt = kt0; kt < kt1; ++kt) {
           if (!ptx::mbar_wait(&full[stage], phase, kWaitLimit)) {
             atomicExch(p.err, kErrMma);
             ok = false;
@@ -230,7 +250,7 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t adesc = ptx::smem_desc(a_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
             const uint64_t bdesc = ptx::smem_desc(b_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
             ptx::tc_mma_nvf4(tmem, adesc, bdesc, Cfg::IDESC, sfa_t + 4u * g,
-                             sfb_t + (uint32_t)(Cfg::SFB_COLS_PER_STEP * g), (kt | g) != 0 ? 1u : 0u);
+                             sfb_t + (uint32_t)(Cfg::SFB_COLS_PER_STEP * g), (kt != kt0 || g != 0) ? 1u : 0u);
           }
           issued = true;
           ptx::tc_commit(&empty[stage]);
@@ -251,29 +271,41 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // epilogue warps: TMEM lane quarter (warp % 4) holds tile rows 32*(warp%4) .. +31
     const int q = warp & 3;
+    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps
     const float alpha = __ldg(p.ts_a) * __ldg(p.ts_b);
     const bool has_add = p.col_add != nullptr;
     const bool has_outer = p.row_vec != nullptr;
     uint8_t* stage_base = smem + Cfg::OFF_EPI + q * 2 * Cfg::EPI_BUF;
+    float* vec_base = reinterpret_cast<float*>(smem + Cfg::OFF_VEC);
+    __shared__ int s_ok[2];
     int sbuf = 0;
     int it = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++it) {
-      const int mt = tile % num_m, nt = tile / num_m;
+      int mt, nt, kt0, kt1;
+      decode(tile, mt, nt, kt0, kt1);
       const int row = mt * Cfg::BM + q * 32 + lane;
       const int row0 = mt * Cfg::BM + q * 32;
       const float rterm = (has_outer && row < p.M) ? p.outer * __ldg(p.row_vec + row) : 0.f;
-      if (!ptx::mbar_wait(tfull, it & 1, kWaitLimit)) {
-        atomicExch(p.err, kErrEpilogue);
+      // this tile's vector entries -> SMEM (double-buffered by tile parity: a warp
+      // reaches the next tile's writes only after every warp passed this barrier)
+      float* cadd_s = vec_base + (it & 1) * 2 * BN;
+      float* cvec_s = cadd_s + BN;
+      for (int c = et; c < BN; c += 128) {
+        const int col = nt * BN + c;
+        cadd_s[c] = (has_add && col < p.N) ? __ldg(p.col_add + col) : 0.f;
+        cvec_s[c] = (has_outer && col < p.N) ? __ldg(p.col_vec + col) : 0.f;
+      }
+      // one thread waits for the accumulator; the barrier hands its verdict (and
+      // the staged vectors) to all four warps, so they leave the loop together
+      if (et == 0) s_ok[it & 1] = ptx::mbar_wait(tfull, it & 1, kWaitLimit) ? 1 : 0;
+      epi_bar();
+      if (!s_ok[it & 1]) {
+        if (et == 0) atomicExch(p.err, kErrEpilogue);
         break;
       }
       ptx::tc_fence_after();
       const uint32_t t_row = tmem + ((uint32_t)(q * 32) << 16);
 
-      // vector entries of the 32 columns starting at c, one per lane
-      auto vec_at = [&](const float* v, int c) -> float {
-        const int col = nt * BN + c + lane;
-        return (v != nullptr && col < p.N) ? __ldg(v + col) : 0.f;
-      };
       // stage one 32-row x 128-byte box in swizzled SMEM and store it with TMA
       auto store_box = [&](const uint4 (&w)[8], int col0) {
         uint8_t* sb = stage_base + sbuf * Cfg::EPI_BUF;
@@ -290,19 +322,27 @@ __global__ void __launch_bounds__(192, 1)
         }
         sbuf ^= 1;
       };
+      auto store_f32 = [&](const float (&f)[32], int c) {
+        uint4 w[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          w[k] = make_uint4(__float_as_uint(f[4 * k]), __float_as_uint(f[4 * k + 1]), __float_as_uint(f[4 * k + 2]),
+                            __float_as_uint(f[4 * k + 3]));
+        store_box(w, nt * BN + c);
+      };
 
       if (BF16_OUT) {
         // whole accumulator -> packed bf16 registers, release TMEM, then store
         uint32_t packed[BN / 2];
 #pragma unroll
         for (int c = 0; c < BN; c += 32) {
-          const float cadd = vec_at(p.col_add, c);
-          const float cvec = vec_at(p.col_vec, c);
           uint32_t v[32];
           ptx::tmem_ld32(t_row + (uint32_t)c, v);
           ptx::tmem_ld_wait();
-          float f[32];
-          epi_math(f, v, alpha, has_add, cadd, has_outer, rterm, cvec);
+          float acc[32], f[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] = alpha * __uint_as_float(v[j]);
+          epi_math(f, acc, has_add, cadd_s + c, has_outer, rterm, cvec_s + c);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
@@ -324,8 +364,6 @@ __global__ void __launch_bounds__(192, 1)
       } else {
 #pragma unroll 1
         for (int c = 0; c < BN; c += 32) {
-          const float cadd = vec_at(p.col_add, c);
-          const float cvec = vec_at(p.col_vec, c);
           uint32_t v[32];
           ptx::tmem_ld32(t_row + (uint32_t)c, v);
           ptx::tmem_ld_wait();
@@ -335,14 +373,11 @@ __global__ void __launch_bounds__(192, 1)
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(tempty);
           }
-          float f[32];
-          epi_math(f, v, alpha, has_add, cadd, has_outer, rterm, cvec);
-          uint4 w[8];
+          float acc[32], f[32];
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            w[k] = make_uint4(__float_as_uint(f[4 * k]), __float_as_uint(f[4 * k + 1]), __float_as_uint(f[4 * k + 2]),
-                              __float_as_uint(f[4 * k + 3]));
-          store_box(w, nt * BN + c);
+          for (int j = 0; j < 32; ++j) acc[j] = alpha * __uint_as_float(v[j]);
+          epi_math(f, acc, has_add, cadd_s + c, has_outer, rterm, cvec_s + c);
+          store_f32(f, c);
         }
       }
     }

@@ -29,10 +29,10 @@
 
 namespace averis {
 
-// Control block at the head of every quantize workspace.  Every word is zero
-// at rest: the stats pass accumulates maxima with atomicMax and resets its
-// strip tickets itself; the last CTA of the quantize pass (ticket) resets the
-// maxima after every reader is done, so a workspace that starts zeroed stays
+// Control block at the head of every workspace.  Every word is zero at rest:
+// the stats pass accumulates maxima with atomicMax and resets its strip
+// tickets itself; the last CTA of the quantize pass (ticket) resets the
+// maxima after every reader is done.  A workspace that starts zeroed stays
 // usable for any later call without a memset.
 enum : int {
   kCtrlAmaxRes = 1,      // residual max magnitude (float bits), both layouts
