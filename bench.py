@@ -481,6 +481,7 @@ def run_ours(args, rank, ws):
         line["quantize_sweep"] = quantize_sweep(peaks)
         line["preprocess_vs_hadamard"] = preprocess_comparison()
         line["stack_28_layers"] = stack_comparison()
+        line["moe_expert_ffn"] = moe_comparison()
         line["quant_error_qkv"] = quant_error_diagnostic(layers[0])
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
@@ -620,6 +621,66 @@ def quant_error_diagnostic(layer):
         res[name] = {"vanilla": round(float(torch.linalg.vector_norm(e_van) / nrm), 5),
                      "averis": round(float(torch.linalg.vector_norm(e_av) / nrm), 5)}
         del ref, van, av, e_van, e_av
+    return res
+
+
+def moe_comparison(steps=3, warmup=2):
+    """Mixture-of-experts expert FFN: hidden 2048, 64 experts, top-8, expert FFN
+    768 (gate_up 2048 -> 1536, down 768 -> 2048), 16384 tokens routed with
+    Zipf(1.1) popularity; the means are per expert over its tokens.  One step is
+    the weight quantize, forward and backward of both grouped linears."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    cfg = workloads.MOE
+    dev = torch.device("cuda", torch.cuda.current_device())
+    counts = workloads.moe_routing(0, cfg["tokens"], cfg["experts"], cfg["top_k"], cfg["zipf"])
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    rows = int(offsets[-1])
+    shapes = (("gate_up", cfg["hidden"], 2 * cfg["ffn"]), ("down", cfg["ffn"], cfg["hidden"]))
+    lin = []
+    for i, (name, m, n) in enumerate(shapes):
+        x = workloads.torch_activation(31 + i, rows, m, spike=workloads.QWEN3_SPIKE, device=dev)
+        _, _, d = workloads.torch_linear_case(41 + i, rows, 16, n, device=dev)
+        w = [workloads.torch_linear_case(100 * i + e, 16, m, n, device=dev)[1] for e in range(cfg["experts"])]
+        wn = [capi.NVFP4Tensor.empty(m, n, dev) for _ in w]
+        wm = [capi.NVFP4Tensor.empty(n, m, dev) for _ in w]
+        gl = capi.GroupedLinear(offsets, m, n, wm, wn, dev)
+        y = torch.empty(rows, n, dtype=torch.bfloat16, device=dev)
+        dx = torch.empty(rows, m, dtype=torch.bfloat16, device=dev)
+        lin.append((m, n, x, d, w, wn, wm, gl, y, dx))
+    lib = capi.load()
+
+    def step(flags):
+        for m, n, x, d, w, wn, wm, gl, y, dx in lin:
+            wsb = capi.workspace(lib.averis_quantize_workspace_bytes(m, n, 0), dev, "moe_wq")
+            for we, a, b in zip(w, wn, wm):
+                sa, sb = a.struct(), b.struct()
+                capi._check(lib.averis_quantize_weight(capi._ptr(we), m, n, 0, ctypes.byref(sa), ctypes.byref(sb),
+                                                       capi._ptr(wsb), wsb.numel(), capi._stream(dev)), "wq")
+            gl.fwd(x, flags, out_bf16=True, y=y)
+            gl.bwd(d, flags, out_bf16=True, dx=dx)
+
+    flops = sum(6.0 * rows * m * n + 5.0 * m * n * cfg["experts"] for m, n, *_ in lin)
+    stream = torch.cuda.current_stream()
+    res = {"experts": cfg["experts"], "top_k": cfg["top_k"], "tokens": cfg["tokens"],
+           "rows_per_expert_max": int(counts.max()), "rows_per_expert_min": int(counts.min()),
+           "gflop_per_step": round(flops / 1e9, 1),
+           "note": "one launch chain per expert (no grouped tile scheduler yet)"}
+    for name, flags in (("nvfp4", 0), ("averis", capi.AVERIS_MEAN_SPLIT)):
+        step(flags)
+        torch.cuda.synchronize()
+        g = capture(lambda flags=flags: step(flags))
+        for _ in range(warmup):
+            g.replay()
+        t = time_graph(g, steps, stream)
+        res[f"ms_{name}"] = round(t, 3)
+        res[f"tflops_{name}"] = round(flops / (t * 1e-3) / 1e12, 1)
+        del g
+    res["overhead_averis"] = round((res["ms_averis"] - res["ms_nvfp4"]) / res["ms_nvfp4"], 4)
+    del lin
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     return res
 
 

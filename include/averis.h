@@ -221,6 +221,39 @@ averis_status nvfp4_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n,
                                void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Grouped (mixture-of-experts) linear layer: the same layer applied to each
+ * expert's own tokens with the expert's own weights ([P1-method] per expert:
+ * the means are taken over that expert's tokens).  The pages train a
+ * Qwen3-7B-A1.5B MoE model with the method (paperlayer.ai summary, section 4
+ * Experiments).
+ *  x / d         device bf16 [L, m] / [L, n], rows grouped by expert: expert e
+ *                owns rows offsets[e] .. offsets[e+1]-1 (L = offsets[E]).
+ *  offsets       HOST array of E+1 non-decreasing row offsets, offsets[0] = 0;
+ *                an expert with no rows is skipped (its state and dW untouched).
+ *  w_m / w_n     HOST arrays of E NVFP4 descriptors (device buffers), as for
+ *                averis_linear_fwd / averis_linear_bwd.
+ *  states        HOST array of E forward states, expert e's sized for its rows.
+ *  y / dx        device [L, n] / [L, m], the rows grouped like x;  dw  HOST
+ *                array of E device pointers to binary32 [m, n].
+ *  workspace     averis_grouped_linear_*_workspace_bytes() bytes (reused by
+ *                the experts in turn, which run one after another on `stream`).
+ *  flags         AVERIS_MEAN_SPLIT (clear: vanilla NVFP4), AVERIS_HADAMARD16,
+ *                AVERIS_OUT_BF16.
+ */
+size_t averis_grouped_linear_fwd_workspace_bytes(const int64_t* offsets, int64_t num_experts, int64_t m,
+                                                 int64_t n, unsigned flags);
+size_t averis_grouped_linear_bwd_workspace_bytes(const int64_t* offsets, int64_t num_experts, int64_t m,
+                                                 int64_t n, unsigned flags);
+averis_status averis_grouped_linear_fwd(const void* x, const int64_t* offsets, int64_t num_experts, int64_t m,
+                                        int64_t n, const averis_nvfp4* w_m, unsigned flags, void* y,
+                                        const averis_fwd_state* states, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+averis_status averis_grouped_linear_bwd(const void* d, const int64_t* offsets, int64_t num_experts, int64_t m,
+                                        int64_t n, const averis_fwd_state* states, const averis_nvfp4* w_n,
+                                        unsigned flags, void* dx, float* const* dw, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * averis_quantize_noalloc -- averis_quantize without a caller-supplied
  * workspace.  The method has no counterpart of this call: it exists for
  * callers that cannot allocate device memory, such as plugin hosts that hand

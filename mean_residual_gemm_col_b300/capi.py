@@ -34,6 +34,8 @@ EXPORTS = (
     "averis_gemm", "averis_linear_fwd_workspace_bytes", "averis_linear_bwd_workspace_bytes",
     "averis_linear_fwd", "averis_linear_bwd", "nvfp4_linear_fwd", "nvfp4_linear_bwd",
     "averis_status_string", "averis_last_device_error", "averis_version", "averis_quantize_noalloc",
+    "averis_grouped_linear_fwd_workspace_bytes", "averis_grouped_linear_bwd_workspace_bytes",
+    "averis_grouped_linear_fwd", "averis_grouped_linear_bwd",
 )
 
 
@@ -78,6 +80,10 @@ def _declare(lib):
         "averis_last_device_error": (I, [P, ctypes.POINTER(I)]),
         "averis_version": (I, []),
         "averis_quantize_noalloc": (I, [P, I64, I64, U, P, NP, P, NP, NP, P]),
+        "averis_grouped_linear_fwd_workspace_bytes": (SZ, [P, I64, I64, I64, U]),
+        "averis_grouped_linear_bwd_workspace_bytes": (SZ, [P, I64, I64, I64, U]),
+        "averis_grouped_linear_fwd": (I, [P, P, I64, I64, I64, P, U, P, P, P, SZ, P]),
+        "averis_grouped_linear_bwd": (I, [P, P, I64, I64, I64, P, P, U, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -355,6 +361,63 @@ def nvfp4_linear_fwd(x, w_m, flags=0, out_bf16=False, state=None, y=None):
 
 def nvfp4_linear_bwd(d, state, w_n, flags=0, out_bf16=False, dx=None, dw=None):
     return _linear_bwd("nvfp4_linear_bwd", d, state, w_n, flags, out_bf16, dx, dw)
+
+
+class GroupedLinear:
+    """Per-expert buffers of a grouped (mixture-of-experts) linear layer.
+
+    ``offsets`` (E+1 ints) split the expert-grouped rows of x [L, m]; weights
+    are per expert.  The host arrays the C entry points take (offsets, weight
+    descriptors, forward states, dW pointers) are built once here.
+    """
+
+    def __init__(self, offsets, m, n, w_m, w_n, device):
+        import torch
+
+        self.offsets = [int(o) for o in offsets]
+        self.E, self.m, self.n = len(self.offsets) - 1, m, n
+        self._off = (ctypes.c_int64 * (self.E + 1))(*self.offsets)
+        self.w_m, self.w_n = w_m, w_n
+        self._wm = (NVFP4Struct * self.E)(*[w.struct() for w in w_m])
+        self._wn = (NVFP4Struct * self.E)(*[w.struct() for w in w_n])
+        self.states = [FwdState.empty(max(1, b - a), m, device) for a, b in zip(self.offsets, self.offsets[1:])]
+        self._st = (FwdStateStruct * self.E)(*[st.struct() for st in self.states])
+        self.dw = [torch.zeros(m, n, dtype=torch.float32, device=device) for _ in range(self.E)]
+        self._dw = (ctypes.c_void_p * self.E)(*[t.data_ptr() for t in self.dw])
+
+    def fwd(self, x, flags=AVERIS_MEAN_SPLIT, out_bf16=False, y=None):
+        import torch
+
+        lib = load()
+        _check_bf16(x, "x")
+        dev = x.device
+        f = flags | (AVERIS_OUT_BF16 if out_bf16 else 0)
+        if y is None:
+            y = torch.empty((self.offsets[-1], self.n), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                            device=dev)
+        ws = workspace(lib.averis_grouped_linear_fwd_workspace_bytes(self._off, self.E, self.m, self.n, f), dev,
+                       "gfwd")
+        _check(lib.averis_grouped_linear_fwd(_ptr(x), self._off, self.E, self.m, self.n, self._wm, f, _ptr(y),
+                                             self._st, _ptr(ws), ws.numel(), _stream(dev)),
+               "averis_grouped_linear_fwd")
+        return y
+
+    def bwd(self, d, flags=AVERIS_MEAN_SPLIT, out_bf16=False, dx=None):
+        import torch
+
+        lib = load()
+        _check_bf16(d, "d")
+        dev = d.device
+        f = flags | (AVERIS_OUT_BF16 if out_bf16 else 0)
+        if dx is None:
+            dx = torch.empty((self.offsets[-1], self.m), dtype=torch.bfloat16 if out_bf16 else torch.float32,
+                             device=dev)
+        ws = workspace(lib.averis_grouped_linear_bwd_workspace_bytes(self._off, self.E, self.m, self.n, f), dev,
+                       "gbwd")
+        _check(lib.averis_grouped_linear_bwd(_ptr(d), self._off, self.E, self.m, self.n, self._st, self._wn, f,
+                                             _ptr(dx), self._dw, _ptr(ws), ws.numel(), _stream(dev)),
+               "averis_grouped_linear_bwd")
+        return dx, self.dw
 
 
 def averis_last_device_error(device=None) -> int:

@@ -530,6 +530,76 @@ averis_status nvfp4_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n, c
                          stream);
 }
 
+// ------------------------------------------------------- grouped (MoE) --
+
+static bool offsets_ok(const int64_t* offsets, int64_t num_experts) {
+  if (offsets == nullptr || num_experts < 1 || offsets[0] != 0) return false;
+  for (int64_t e = 0; e < num_experts; ++e)
+    if (offsets[e + 1] < offsets[e]) return false;
+  return true;
+}
+
+size_t averis_grouped_linear_fwd_workspace_bytes(const int64_t* offsets, int64_t num_experts, int64_t m, int64_t n,
+                                                 unsigned flags) {
+  (void)flags;
+  if (!offsets_ok(offsets, num_experts) || m < 1 || n < 1) return 0;
+  size_t b = 0;
+  for (int64_t e = 0; e < num_experts; ++e) {
+    const int64_t le = offsets[e + 1] - offsets[e];
+    if (le > 0) b = std::max(b, fwd_ws(le, m, n));
+  }
+  return std::max<size_t>(b, 256);
+}
+
+size_t averis_grouped_linear_bwd_workspace_bytes(const int64_t* offsets, int64_t num_experts, int64_t m, int64_t n,
+                                                 unsigned flags) {
+  (void)flags;
+  if (!offsets_ok(offsets, num_experts) || m < 1 || n < 1) return 0;
+  size_t b = 0;
+  for (int64_t e = 0; e < num_experts; ++e) {
+    const int64_t le = offsets[e + 1] - offsets[e];
+    if (le > 0) b = std::max(b, bwd_ws(le, m, n));
+  }
+  return std::max<size_t>(b, 256);
+}
+
+averis_status averis_grouped_linear_fwd(const void* x, const int64_t* offsets, int64_t num_experts, int64_t m,
+                                        int64_t n, const averis_nvfp4* w_m, unsigned flags, void* y,
+                                        const averis_fwd_state* states, void* workspace, size_t workspace_bytes,
+                                        cudaStream_t stream) {
+  if (x == nullptr || y == nullptr || w_m == nullptr || states == nullptr) return AVERIS_ERR_INVALID_ARG;
+  if (!offsets_ok(offsets, num_experts)) return AVERIS_ERR_INVALID_ARG;
+  const int64_t esz = (flags & AVERIS_OUT_BF16) ? 2 : 4;
+  for (int64_t e = 0; e < num_experts; ++e) {
+    const int64_t r0 = offsets[e], le = offsets[e + 1] - offsets[e];
+    if (le == 0) continue;
+    const averis_status st = linear_fwd_impl(static_cast<const uint8_t*>(x) + r0 * m * 2, le, m, n, &w_m[e], flags,
+                                             static_cast<uint8_t*>(y) + r0 * n * esz, &states[e], workspace,
+                                             workspace_bytes, stream);
+    if (st != AVERIS_OK) return st;
+  }
+  return AVERIS_OK;
+}
+
+averis_status averis_grouped_linear_bwd(const void* d, const int64_t* offsets, int64_t num_experts, int64_t m,
+                                        int64_t n, const averis_fwd_state* states, const averis_nvfp4* w_n,
+                                        unsigned flags, void* dx, float* const* dw, void* workspace,
+                                        size_t workspace_bytes, cudaStream_t stream) {
+  if (d == nullptr || dx == nullptr || dw == nullptr || w_n == nullptr || states == nullptr)
+    return AVERIS_ERR_INVALID_ARG;
+  if (!offsets_ok(offsets, num_experts)) return AVERIS_ERR_INVALID_ARG;
+  const int64_t esz = (flags & AVERIS_OUT_BF16) ? 2 : 4;
+  for (int64_t e = 0; e < num_experts; ++e) {
+    const int64_t r0 = offsets[e], le = offsets[e + 1] - offsets[e];
+    if (le == 0) continue;
+    const averis_status st = linear_bwd_impl(static_cast<const uint8_t*>(d) + r0 * n * 2, le, m, n, &states[e],
+                                             &w_n[e], flags, static_cast<uint8_t*>(dx) + r0 * m * esz, dw[e],
+                                             workspace, workspace_bytes, stream);
+    if (st != AVERIS_OK) return st;
+  }
+  return AVERIS_OK;
+}
+
 const char* averis_status_string(averis_status status) {
   switch (status) {
     case AVERIS_OK: return "ok";

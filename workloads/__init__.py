@@ -115,6 +115,18 @@ def linear_case(seed: int, l: int, m: int, n: int, *, spike=50.0) -> LinearCase:
     return LinearCase(activation(g, l, m, spike=spike), weight(g, m, n), output_grad(g, l, n))
 
 
+def moe_routing(seed: int, tokens: int, experts: int, top_k: int, zipf: float) -> np.ndarray:
+    """Rows per expert when each token picks ``top_k`` distinct experts with
+    probability proportional to rank^(-zipf) (expert e has rank e + 1):
+    Gumbel-top-k sampling with NumPy PCG64.  Returns int64 [experts] counts
+    (they sum to tokens * top_k); expert-grouped rows are their prefix sums."""
+    g = rng(seed)
+    logp = -zipf * np.log(np.arange(1, experts + 1, dtype=np.float64))
+    keys = logp[None, :] + g.gumbel(size=(tokens, experts))
+    picks = np.argpartition(-keys, top_k - 1, axis=1)[:, :top_k]
+    return np.bincount(picks.ravel(), minlength=experts).astype(np.int64)
+
+
 # ------------------------------------------------------ torch backend ----
 
 def torch_linear_case(seed: int, l: int, m: int, n: int, *, spike=50.0, device="cuda"):
