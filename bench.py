@@ -375,9 +375,15 @@ def run_ours(args, rank, ws):
     for _ in range(args.warmup):
         for m in ("nvfp4", "averis_h16", "nvfp4_h16"):
             graphs[m].replay()
-    ms_van = max_over_ranks(time_graph(graphs["nvfp4"], args.steps, stream), ws)
-    ms_had = max_over_ranks(time_graph(graphs["averis_h16"], args.steps, stream), ws)
-    ms_vhad = max_over_ranks(time_graph(graphs["nvfp4_h16"], args.steps, stream), ws)
+    def timed(mode):
+        torch.cuda.nvtx.range_push(f"{mode}_timed")
+        t = time_graph(graphs[mode], args.steps, stream)
+        torch.cuda.nvtx.range_pop()
+        return max_over_ranks(t, ws)
+
+    ms_van = timed("nvfp4")
+    ms_had = timed("averis_h16")
+    ms_vhad = timed("nvfp4_h16")
     kern = {}
     for k, g in ggraphs.items():
         g.replay()
