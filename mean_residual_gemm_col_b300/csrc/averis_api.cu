@@ -109,10 +109,12 @@ StatsGeom stats_geom(int64_t R, int64_t C) {
   StatsGeom g;
   g.nstrips = (int)cdiv(C, 64);
   g.gx = std::min(g.nstrips, (int)kMaxStripGroups);
-  int64_t nrb = cdiv(kStatsTargetCtas, g.gx);
-  nrb = std::max<int64_t>(1, std::min<int64_t>(nrb, cdiv(R, 512)));  // at least 2 load groups per thread
+  // one wave of CTAs (2 per SM), each at least 256 rows (8 per thread), row
+  // blocks balanced to a multiple of 32 rows
+  int64_t nrb = std::max<int64_t>(1, kStatsTargetCtas / g.gx);
+  nrb = std::max<int64_t>(1, std::min<int64_t>(nrb, cdiv(R, 256)));
   int64_t rp = cdiv(R, nrb);
-  rp = cdiv(rp, 256) * 256;
+  rp = cdiv(rp, 32) * 32;
   g.rows_per = rp;
   g.nrb = (int)cdiv(R, rp);
   return g;

@@ -577,14 +577,17 @@ struct QuantParams {
 
 constexpr int kQTile = 128;
 constexpr int kQThreads = 256;
+constexpr int kQWarps = kQThreads / 32;
 constexpr int kQBufs = 3;                         // tile buffers per CTA
 constexpr int kQHalf = kQTile * 64 * 2;          // one 128-row x 64-column bf16 box (16 KB)
 constexpr int kQTileBytes = 2 * kQHalf;           // 32 KB
-// SMEM: tile buffers | mu [kQBufs][128] | inverse-scale tables [2][128] | column-layout scale atoms [1 KB] | barriers
+// SMEM: tile buffers | mu [kQBufs][128] | inverse-scale tables [2][128] |
+// scale-atom staging [kQBufs][row atoms 1 KB | column atoms 1 KB] | barriers, counters
 constexpr int kQOffMu = kQBufs * kQTileBytes;
 constexpr int kQOffInv = kQOffMu + kQBufs * 128 * 4;
-constexpr int kQOffCs = kQOffInv + 2 * 128 * 4;
-constexpr int kQOffBar = kQOffCs + 1024;
+constexpr int kQOffStage = kQOffInv + 2 * 128 * 4;
+constexpr int kQStageBytes = 2048;
+constexpr int kQOffBar = kQOffStage + kQBufs * kQStageBytes;
 constexpr int kQSmem = kQOffBar + 64 + 1024;      // + alignment slack
 
 // inv(e) = min(fl32(1 / fl32(e4m3(e) s_g)), FLT_MAX), or 0 when the decode scale is 0.
@@ -603,6 +606,20 @@ __device__ __forceinline__ float absmax16(const float (&r)[16]) {
   return fmaxf(a0, a1);
 }
 
+// Eight binary32 values (four packed pairs, element 0 in the low half of q[0])
+// -> eight E2M1 codes in one word, element 0 in the low nibble.
+__device__ __forceinline__ uint32_t e2m1x8(uint64_t q0, uint64_t q1, uint64_t q2, uint64_t q3) {
+  uint32_t out;
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n .reg .f32 l0, h0, l1, h1, l2, h2, l3, h3;\n"
+      " mov.b64 {l0, h0}, %1;\n mov.b64 {l1, h1}, %2;\n mov.b64 {l2, h2}, %3;\n mov.b64 {l3, h3}, %4;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b0, h0, l0;\n cvt.rn.satfinite.e2m1x2.f32 b1, h1, l1;\n"
+      " cvt.rn.satfinite.e2m1x2.f32 b2, h2, l2;\n cvt.rn.satfinite.e2m1x2.f32 b3, h3, l3;\n"
+      " mov.b32 %0, {b0, b1, b2, b3};\n}"
+      : "=r"(out)
+      : "l"(q0), "l"(q1), "l"(q2), "l"(q3));
+  return out;
+}
+
 // NVFP4 of one 16-element block with a per-tensor table of reciprocal decode
 // scales (same binary32 steps as quant_block16).  Returns the E4M3 code.
 __device__ __forceinline__ uint32_t quant16_tab(const float (&r)[16], float den, bool s_pos, const float* inv_tab,
@@ -611,167 +628,133 @@ __device__ __forceinline__ uint32_t quant16_tab(const float (&r)[16], float den,
   const uint32_t code = s_pos ? ptx::cvt_e4m3(__fdiv_rn(a, den)) : 0u;
   const float inv = inv_tab[code];
   const uint64_t inv2 = f2pack(inv, inv);
-  uint32_t w[2] = {0u, 0u};
+  uint64_t q[8];
 #pragma unroll
-  for (int e = 0; e < 8; ++e) {
-    const uint64_t q = mul2(f2pack(r[2 * e], r[2 * e + 1]), inv2);
-    w[e >> 2] |= ptx::cvt_e2m1x2(f2lo(q), f2hi(q)) << (8 * (e & 3));
-  }
-  lo = w[0];
-  hi = w[1];
+  for (int e = 0; e < 8; ++e) q[e] = mul2(f2pack(r[2 * e], r[2 * e + 1]), inv2);
+  lo = e2m1x8(q[0], q[1], q[2], q[3]);
+  hi = e2m1x8(q[4], q[5], q[6], q[7]);
   return code;
 }
 
-// Blocks along C (row layout).  Warps 0-3; lane = (block pair bq = lane / 8,
-// row rr = 8 * warp + lane % 8): blocks 2bq, 2bq+1 (tile columns 32bq..32bq+31)
-// of tile rows rr, rr+32, rr+64, rr+96.  The tile sits in SMEM as two
-// 64-column halves of 128 rows x 128 bytes, 16-byte chunk j of row r at chunk
-// j ^ (r % 8) (the TMA 128-byte swizzle): the 8 lanes of a load phase read 8
-// different rows at distinct banks.
-template <bool AMAX_ONLY>
-__device__ __forceinline__ void quant_rows(const QuantParams& p, const uint8_t* buf, const float* mu_s, int64_t r0,
-                                           int64_t c0, int tr, int tc, bool split, float den, bool s_pos,
-                                           const float* inv_tab, float& amax) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int bq = lane >> 3, rr = 8 * warp + (lane & 7);
-  const uint8_t* half = buf + (bq >> 1) * kQHalf;
-  const int ch0 = 4 * (bq & 1);
-  float m[32];
+// One 128 x 128 tile, both layouts, by one warp: warp w owns tile rows
+// 32(w/2) .. +31 of the 64-column half w%2 (exactly one TMA box).  The box
+// sits in SMEM as 128 rows x 128 bytes, 16-byte chunk j of row r at chunk
+// j ^ (r % 8) (the TMA 128-byte swizzle).
+//
+// Blocks along C (row layout): lane = (block kb = lane % 4, row rs = lane / 4);
+// rows rs, rs + 8, rs + 16, rs + 24 of the warp's 32.  A quarter-warp reads
+// 2 rows x 4 blocks: 8 distinct chunk positions, no bank conflict.
+// Blocks along R (column layout): lane = (column quad cq = lane % 16, row
+// block rb = lane / 16); 4 columns x 16 rows.  Each half-warp reads one full
+// 128-byte row per load: no bank conflict.
+// Codes go to global memory directly; block scales to the SMEM staging of
+// this buffer (the tile fills exactly two 512-byte atoms of each layout).
+// EDGE: the tile crosses row R or column C (masked, zero-filled blocks).
+template <bool AMAX_ONLY, bool EDGE>
+__device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint8_t* buf, const float* mub,
+                                                uint8_t* stage, int64_t r0, int64_t c0, float den_row, float den_col,
+                                                bool pos_row, bool pos_col, const float* inv_s, bool rows_on,
+                                                bool cols_on, float& amax_row, float& amax_col) {
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int half = w & 1, rq = w >> 1;
+  const uint8_t* hb = buf + half * kQHalf;
+  const float* mh = mub + 64 * half;
+  const int64_t ch = c0 + 64 * half;  // first column of the half
+  if (rows_on) {
+    const int kb = lane & 3, rs = lane >> 2;
+    uint64_t m2[8];
 #pragma unroll
-  for (int k = 0; k < 32; k += 4) {
-    const float4 m4 = split ? *reinterpret_cast<const float4*>(mu_s + 32 * bq + k) : make_float4(0.f, 0.f, 0.f, 0.f);
-    m[k] = m4.x;
-    m[k + 1] = m4.y;
-    m[k + 2] = m4.z;
-    m[k + 3] = m4.w;
-  }
-  const bool cvalid0 = c0 + 32 * bq < p.C, cvalid1 = c0 + 32 * bq + 16 < p.C;
-#pragma unroll 1
-  for (int pp = 0; pp < 4; ++pp) {
-    const int row = rr + 32 * pp;
-    const int64_t gr = r0 + row;
-    const bool rvalid = gr < p.R;
-    uint4 v[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) v[k] = *reinterpret_cast<const uint4*>(half + row * 128 + (((ch0 + k) ^ (row & 7)) << 4));
-    uint32_t code[4];
-    uint32_t sc = 0;
-#pragma unroll
-    for (int b = 0; b < 2; ++b) {
-      const uint32_t wv[8] = {v[2 * b].x, v[2 * b].y, v[2 * b].z, v[2 * b].w,
-                              v[2 * b + 1].x, v[2 * b + 1].y, v[2 * b + 1].z, v[2 * b + 1].w};
+    for (int k = 0; k < 4; ++k) {
+      const float4 m4 = *reinterpret_cast<const float4*>(mh + 16 * kb + 4 * k);
+      m2[2 * k] = f2pack(m4.x, m4.y);
+      m2[2 * k + 1] = f2pack(m4.z, m4.w);
+    }
+    const bool cvalid = !EDGE || ch + 16 * kb < p.C;
+#pragma unroll 2
+    for (int i = 0; i < 4; ++i) {
+      const int row = 32 * rq + rs + 8 * i;
+      const int64_t gr = r0 + row;
+      const uint4 v0 = *reinterpret_cast<const uint4*>(hb + row * 128 + (((2 * kb) ^ (row & 7)) << 4));
+      const uint4 v1 = *reinterpret_cast<const uint4*>(hb + row * 128 + (((2 * kb + 1) ^ (row & 7)) << 4));
+      const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       float rx[16];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint64_t d = split ? sub2(bf2_to_f2(wv[e]), f2pack(m[16 * b + 2 * e], m[16 * b + 2 * e + 1]))
-                                 : bf2_to_f2(wv[e]);
+        const uint64_t d = sub2(bf2_to_f2(wv[e]), m2[e]);
         rx[2 * e] = f2lo(d);
         rx[2 * e + 1] = f2hi(d);
       }
-      if (!rvalid || !(b ? cvalid1 : cvalid0)) {
+      const bool valid = !EDGE || (cvalid && gr < p.R);
+      if (EDGE && !valid) {
 #pragma unroll
         for (int e = 0; e < 16; ++e) rx[e] = 0.f;
       }
       if (p.hadamard) fwht16(rx);
       if (AMAX_ONLY) {
-        amax = fmaxf(amax, absmax16(rx));
+        amax_row = fmaxf(amax_row, absmax16(rx));
       } else {
-        sc |= quant16_tab(rx, den, s_pos, inv_tab, code[2 * b], code[2 * b + 1]) << (8 * b);
+        uint32_t lo, hi;
+        const uint32_t sc = quant16_tab(rx, den_row, pos_row, inv_s, lo, hi);
+        if (valid) *reinterpret_cast<uint2*>(p.row_codes + gr * p.row_ld + ch / 2 + 8 * kb) = make_uint2(lo, hi);
+        stage[half * 512 + 16 * (row & 31) + 4 * (row >> 5) + kb] = (uint8_t)sc;
       }
     }
-    if (AMAX_ONLY) continue;
-    const int64_t boff = c0 / 2 + 16 * bq;
-    if (rvalid && boff < p.row_ld)
-      *reinterpret_cast<uint4*>(p.row_codes + gr * p.row_ld + boff) = make_uint4(code[0], code[1], code[2], code[3]);
-    const int64_t kc = 2 * (int64_t)tc + (bq >> 1);
-    if (kc < p.row_kc)
-      *reinterpret_cast<uint16_t*>(p.row_scales + ((int64_t)tr * p.row_kc + kc) * 512 + 16 * (row & 31) +
-                                   4 * (row >> 5) + 2 * (bq & 1)) = (uint16_t)sc;
   }
-}
-
-// Blocks along R (column layout): warp w (4..7 -> 0..3) owns tile columns
-// 32w..32w+31; lane = (column quad cq = lane % 8, row block rbl = lane / 8);
-// two units per lane (row blocks rbl and rbl + 4), each 4 columns x 16 rows.
-// Codes go straight to global memory (4 lanes fill one 32-byte sector),
-// block scales to the SMEM atom staging `cs`.
-template <bool AMAX_ONLY>
-__device__ __forceinline__ void quant_cols(const QuantParams& p, const uint8_t* buf, const float* mu_s, int64_t r0,
-                                           int64_t c0, bool split, float den, bool s_pos, const float* inv_tab,
-                                           uint8_t* cs, float& amax) {
-  const int w = (threadIdx.x >> 5) - 4, lane = threadIdx.x & 31;
-  const int cq = lane & 7, rbl = lane >> 3;
-  const int cc0 = 32 * w + 4 * cq;                       // first of this lane's 4 tile columns
-  const uint8_t* half = buf + (w >> 1) * kQHalf;
-  const int c16 = 4 * (w & 1) + (cq >> 1), sub = 8 * (cq & 1);
-  float m[4] = {0.f, 0.f, 0.f, 0.f};
-  if (split) {
-    const float4 m4 = *reinterpret_cast<const float4*>(mu_s + cc0);
-    m[0] = m4.x;
-    m[1] = m4.y;
-    m[2] = m4.z;
-    m[3] = m4.w;
-  }
-#pragma unroll 1
-  for (int u = 0; u < 2; ++u) {
-    const int rb = rbl + 4 * u;
-    const bool rows_partial = r0 + 16 * rb + 16 > p.R;
+  if (cols_on) {
+    const int cq = lane & 15, rb = lane >> 4;
+    const int row0 = 32 * rq + 16 * rb;  // first tile row of this lane's blocks
+    const float4 m4 = *reinterpret_cast<const float4*>(mh + 4 * cq);
+    const float mc[4] = {m4.x, m4.y, m4.z, m4.w};
     uint2 x[16];
 #pragma unroll
     for (int e = 0; e < 16; ++e) {
-      const int row = 16 * rb + e;
-      x[e] = *reinterpret_cast<const uint2*>(half + row * 128 + ((c16 ^ (row & 7)) << 4) + sub);
+      const int row = row0 + e;
+      x[e] = *reinterpret_cast<const uint2*>(hb + row * 128 + (((cq >> 1) ^ (row & 7)) << 4) + 8 * (cq & 1));
     }
+    const int64_t off = (r0 + row0) / 2;  // code byte offset of the block within a column
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
+      const uint64_t mm = f2pack(mc[j], mc[j]);
       float rx[16];
 #pragma unroll
       for (int e = 0; e < 16; e += 2) {
         const uint32_t wa = (j >> 1) ? x[e].y : x[e].x;
         const uint32_t wb = (j >> 1) ? x[e + 1].y : x[e + 1].x;
-        const float xa = (j & 1) ? bf16hi(wa) : bf16lo(wa);
-        const float xb = (j & 1) ? bf16hi(wb) : bf16lo(wb);
-        if (split) {
-          const uint64_t d = sub2(f2pack(xa, xb), f2pack(m[j], m[j]));
-          rx[e] = f2lo(d);
-          rx[e + 1] = f2hi(d);
-        } else {
-          rx[e] = xa;
-          rx[e + 1] = xb;
-        }
+        const uint64_t d = sub2(f2pack((j & 1) ? bf16hi(wa) : bf16lo(wa), (j & 1) ? bf16hi(wb) : bf16lo(wb)), mm);
+        rx[e] = f2lo(d);
+        rx[e + 1] = f2hi(d);
       }
-      const int cc = cc0 + j;
-      const bool cvalid = c0 + cc < p.C;
-      if (!cvalid) {
-#pragma unroll
-        for (int e = 0; e < 16; ++e) rx[e] = 0.f;
-      } else if (rows_partial) {
+      const int cc = 64 * half + 4 * cq + j;  // tile column
+      const bool cvalid = !EDGE || c0 + cc < p.C;
+      if (EDGE) {
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          if (r0 + 16 * rb + e >= p.R) rx[e] = 0.f;
+          if (!cvalid || r0 + row0 + e >= p.R) rx[e] = 0.f;
       }
       if (p.hadamard) fwht16(rx);
       if (AMAX_ONLY) {
-        amax = fmaxf(amax, absmax16(rx));
+        amax_col = fmaxf(amax_col, absmax16(rx));
       } else {
         uint32_t lo, hi;
-        const uint32_t s = quant16_tab(rx, den, s_pos, inv_tab, lo, hi);
-        const int64_t off = r0 / 2 + 8 * rb;
-        if (cvalid && off < p.col_ld)
+        const uint32_t sc = quant16_tab(rx, den_col, pos_col, inv_s + 128, lo, hi);
+        if (cvalid && (!EDGE || off < p.col_ld))
           *reinterpret_cast<uint2*>(p.col_codes + (c0 + cc) * p.col_ld + off) = make_uint2(lo, hi);
-        cs[(rb >> 2) * 512 + 16 * (cc & 31) + 4 * (cc >> 5) + (rb & 3)] = (uint8_t)s;
+        stage[1024 + (rq >> 1) * 512 + 16 * (cc & 31) + 4 * (cc >> 5) + 2 * (rq & 1) + rb] = (uint8_t)sc;
       }
     }
   }
 }
 
 // Split + quantize, both layouts from one read of each 128 x 128 tile.
-// Persistent CTAs with kQBufs tile buffers filled by TMA (mbarrier-tracked);
-// warps 0-3 write the row layout and warps 4-7 the column layout of the
-// same tile; the last CTA also quantizes the mean, and the last CTA to finish
-// resets the control block's maxima.  AMAX_ONLY: compute the rotated
-// residual's per-layout maximum magnitude (Hadamard variant) instead of
-// quantizing.
+// Persistent CTAs with kQBufs tile buffers, each filled by TMA together with
+// the tile's 128 mean values (bulk copy) on one mbarrier.  Every warp does
+// the same share of every tile (both layouts of a 32 x 64 sub-tile) and
+// counts itself done in the buffer's counter; the warp that completes the
+// count writes the tile's four staged scale atoms and refills the buffer.
+// Dedicated CTAs quantize the mean and compute the rank-one row; the last
+// CTA to finish resets the control block's maxima.  AMAX_ONLY: compute the
+// rotated residual's per-layout maximum magnitude (Hadamard variant)
+// instead of quantizing.
 template <bool AMAX_ONLY>
 __global__ void __launch_bounds__(kQThreads, 2)
     split_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
@@ -779,12 +762,11 @@ __global__ void __launch_bounds__(kQThreads, 2)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
   float* mu_s = reinterpret_cast<float*>(sm + kQOffMu);
   float* inv_s = reinterpret_cast<float*>(sm + kQOffInv);
-  uint8_t* cs = sm + kQOffCs;
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kQOffBar);
+  int* done = reinterpret_cast<int*>(sm + kQOffBar + 8 * kQBufs);
   __shared__ float red[8];
-  __shared__ int s_flag;
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, lane = tid & 31;
   const int ntiles = p.tiles_r * p.tiles_c;
   const bool split = p.mu != nullptr;
   const bool mean_cta = (int)blockIdx.x < p.mean_ctas;
@@ -792,12 +774,22 @@ __global__ void __launch_bounds__(kQThreads, 2)
   const bool rows_on = AMAX_ONLY || p.row_codes != nullptr;
   const bool cols_on = AMAX_ONLY || p.col_codes != nullptr;
 
-  auto issue = [&](int tile, int b) {
+  auto mu_bytes = [&](int tile) {
+    const int64_t left = p.C - (int64_t)(tile % p.tiles_c) * kQTile;
+    return (uint32_t)(left < kQTile ? left : kQTile) * 4u;
+  };
+  auto issue_x = [&](int tile, int b) {
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
-    ptx::mbar_arrive_expect_tx(&full[b], (uint32_t)kQTileBytes);
+    ptx::mbar_arrive_expect_tx(&full[b], (uint32_t)kQTileBytes + (split ? mu_bytes(tile) : 0u));
     ptx::tma_load_2d(sm + b * kQTileBytes, &tmX, tc * kQTile, tr * kQTile, &full[b]);
     ptx::tma_load_2d(sm + b * kQTileBytes + kQHalf, &tmX, tc * kQTile + 64, tr * kQTile, &full[b]);
   };
+  auto issue_mu = [&](int tile, int b) {
+    if (split) ptx::bulk_load(mu_s + 128 * b, p.mu + (int64_t)(tile % p.tiles_c) * kQTile, mu_bytes(tile), &full[b]);
+  };
+  if (tid < kQBufs) done[tid] = 0;
+  if (!split)
+    for (int k = tid; k < kQBufs * 128; k += kQThreads) mu_s[k] = 0.f;  // x - 0 = x exactly
   if (tid == 0) {
     for (int b = 0; b < kQBufs; ++b) ptx::mbar_init(&full[b], 1);
     ptx::fence_mbar_init();
@@ -805,9 +797,12 @@ __global__ void __launch_bounds__(kQThreads, 2)
     // the input was written before the previous kernel started: fetch while it finishes
     if (!mean_cta)
       for (int b = 0; b < kQBufs; ++b)
-        if (tcta + b * ntcta < ntiles) issue(tcta + b * ntcta, b);
+        if (tcta + b * ntcta < ntiles) issue_x(tcta + b * ntcta, b);
   }
   ptx::pdl_wait_and_release();
+  if (tid == 0 && !mean_cta)
+    for (int b = 0; b < kQBufs; ++b)
+      if (tcta + b * ntcta < ntiles) issue_mu(tcta + b * ntcta, b);  // the mean comes from the stats pass
 
   float s_row = 0.f, s_col = 0.f;
   if (!AMAX_ONLY) {
@@ -823,6 +818,7 @@ __global__ void __launch_bounds__(kQThreads, 2)
       if (p.col_ts) *p.col_ts = s_col;
     }
   }
+  __syncthreads();  // tables, counters, barrier init
   const float den_row = __fmul_rn(6.0f, s_row), den_col = __fmul_rn(6.0f, s_col);
   float amax_row = 0.f, amax_col = 0.f;
   if (!AMAX_ONLY && split && mean_cta) {
@@ -842,28 +838,54 @@ __global__ void __launch_bounds__(kQThreads, 2)
     const int b = i % kQBufs;
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     const int64_t r0 = (int64_t)tr * kQTile, c0 = (int64_t)tc * kQTile;
-    float* mub = mu_s + 128 * b;
-    if (tid < 128) mub[tid] = (split && c0 + tid < p.C) ? __ldg(p.mu + c0 + tid) : 0.f;
-    if (tid == 0) s_flag = ptx::mbar_wait(&full[b], (uint32_t)((i / kQBufs) & 1), kWaitLimit) ? 1 : 0;
-    __syncthreads();
-    if (!s_flag) {
-      if (tid == 0) atomicExch(p.err, kErrQuantLoad);
+    if (!ptx::mbar_wait(&full[b], (uint32_t)((i / kQBufs) & 1), kWaitLimit)) {
+      if (lane == 0) atomicExch(p.err, kErrQuantLoad);
       break;
     }
     const uint8_t* buf = sm + b * kQTileBytes;
-    if (warp < 4) {
-      if (rows_on) quant_rows<AMAX_ONLY>(p, buf, mub, r0, c0, tr, tc, split, den_row, s_row > 0.f, inv_s, amax_row);
-    } else if (cols_on) {
-      quant_cols<AMAX_ONLY>(p, buf, mub, r0, c0, split, den_col, s_col > 0.f, inv_s + 128, cs, amax_col);
+    uint8_t* stage = sm + kQOffStage + b * kQStageBytes;
+    const float* mub = mu_s + 128 * b;
+    if (r0 + kQTile > p.R || c0 + kQTile > p.C)
+      quant_tile_warp<AMAX_ONLY, true>(p, buf, mub, stage, r0, c0, den_row, den_col, s_row > 0.f, s_col > 0.f, inv_s,
+                                       rows_on, cols_on, amax_row, amax_col);
+    else
+      quant_tile_warp<AMAX_ONLY, false>(p, buf, mub, stage, r0, c0, den_row, den_col, s_row > 0.f, s_col > 0.f,
+                                        inv_s, rows_on, cols_on, amax_row, amax_col);
+    // count this warp done with the buffer; the last of the kQWarps writes the
+    // staged scale atoms, then refills the buffer (its own reads are done too)
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) {
+      __threadfence_block();
+      last = atomicAdd(&done[b], 1) == kQWarps - 1;
+      if (last) {
+        done[b] = 0;
+        __threadfence_block();
+      }
     }
-    __syncthreads();  // the tile buffer and the scale staging are complete
-    if (tid == 0 && tile + kQBufs * ntcta < ntiles) issue(tile + kQBufs * ntcta, b);
-    if (!AMAX_ONLY && p.col_codes != nullptr && tid < 64) {
-      // column-layout scale atoms: row chunk tc, chunks 2*tr and 2*tr + 1
-      const int64_t kc = 2 * (int64_t)tr + (tid >> 5);
-      if (kc < p.col_kc)
-        *reinterpret_cast<uint4*>(p.col_scales + ((int64_t)tc * p.col_kc + kc) * 512 + 16 * (tid & 31)) =
-            *reinterpret_cast<const uint4*>(cs + 16 * tid);
+    last = __shfl_sync(0xffffffffu, last, 0);
+    if (last) {
+      __syncwarp();
+      if (!AMAX_ONLY) {
+        // 4 atoms x 512 B: row layout (row chunk tr, column chunks 2tc, 2tc+1),
+        // column layout (row chunk tc, column chunks 2tr, 2tr+1)
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const bool is_col = a >= 2;
+          const int64_t kc = (is_col ? 2 * (int64_t)tr : 2 * (int64_t)tc) + (a & 1);
+          const bool on = is_col ? (p.col_codes != nullptr && kc < p.col_kc) : (p.row_codes != nullptr && kc < p.row_kc);
+          if (on) {
+            uint8_t* dst = is_col ? p.col_scales + ((int64_t)tc * p.col_kc + kc) * 512
+                                  : p.row_scales + ((int64_t)tr * p.row_kc + kc) * 512;
+            *reinterpret_cast<uint4*>(dst + 16 * lane) = *reinterpret_cast<const uint4*>(stage + 512 * a + 16 * lane);
+          }
+        }
+        __syncwarp();
+      }
+      if (lane == 0 && tile + kQBufs * ntcta < ntiles) {
+        issue_x(tile + kQBufs * ntcta, b);
+        issue_mu(tile + kQBufs * ntcta, b);
+      }
     }
   }
   if (AMAX_ONLY) {
