@@ -267,7 +267,7 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   const int ntiles = qp.tiles_r * qp.tiles_c;
   // all CTAs resident at once (2 per SM): tile CTAs fill what the mean CTAs leave
   const int tile_ctas =
-      ntiles == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, 2 * (int64_t)dev->sms - qp.mean_ctas));
+      ntiles == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, kQCtasPerSm * (int64_t)dev->sms - qp.mean_ctas));
   if (had) {
     QuantParams ap = qp;  // rotated-maximum pass: tiles only
     ap.mean_ctas = 0;
@@ -345,8 +345,8 @@ averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const floa
   p.early_start = early_start ? 1 : 0;
   const int64_t ntiles = cdiv(M, Cfg::BM) * cdiv(N, BN);
   const int grid = (int)std::min<int64_t>(ntiles, dev->sms);
-  cudaError_t e = bf16 ? launch_pdl(gemm_nvfp4_kernel<true>, dim3(grid), dim3(192), Cfg::SMEM, s, ta, tb, td, p)
-                       : launch_pdl(gemm_nvfp4_kernel<false>, dim3(grid), dim3(192), Cfg::SMEM, s, ta, tb, td, p);
+  cudaError_t e = bf16 ? launch_pdl(gemm_nvfp4_kernel<true>, dim3(grid), dim3(kGemmThreads), Cfg::SMEM, s, ta, tb, td, p)
+                       : launch_pdl(gemm_nvfp4_kernel<false>, dim3(grid), dim3(kGemmThreads), Cfg::SMEM, s, ta, tb, td, p);
   return e == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA;
 }
 

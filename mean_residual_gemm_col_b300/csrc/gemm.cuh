@@ -16,10 +16,17 @@
 // (128 bytes of codes per row), a 3-deep shared-memory ring.  Warp roles:
 //   warp 0     TMA producer: codes by 2-D tensor TMA (128-byte swizzle),
 //              block scales by 1-D bulk copies.
-//   warp 1     TMEM owner and MMA issuer: scale chunks SMEM->TMEM with
-//              tcgen05.cp, then tcgen05.mma kind::mxf4nvf4 128x256x64
-//              accumulating in TMEM; tcgen05.commit frees the stage and,
-//              after the last K tile, hands the accumulator to the epilogue.
+//   warp 1     TMEM owner and MMA issuer: tcgen05.mma kind::mxf4nvf4
+//              128x256x64 accumulating in TMEM; tcgen05.commit frees the
+//              stage and, after the last K tile, hands the accumulator to
+//              the epilogue.
+//   warps 6-9  scale feed: each writes a whole stage's block scales into
+//              its TMEM lane quarter with two tcgen05.st (registers -> TMEM),
+//              the same words a 32x128b.warpx4 copy of each SMEM scale atom
+//              would place there (lane 32 w + i, columns base_g .. +3 = atom
+//              row i).  This keeps the tensor pipe free of the 12 SMEM->TMEM
+//              copies per stage that would otherwise issue between the MMAs
+//              (each costs about as much tensor-pipe time as an MMA).
 //   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, alpha scaling and
 //              the rank-one terms in binary32 (vector entries fetched once
 //              per 32 columns and broadcast by warp shuffles), SMEM staging
@@ -116,27 +123,31 @@ __device__ __forceinline__ void epi_math(float (&f)[32], const float (&acc)[32],
 // Named barrier of the four epilogue warps (ids 1 and up are free for this).
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
+constexpr int kGemmThreads = 320;  // producer, MMA, 4 epilogue warps, 4 scale-feed warps
+
 template <bool BF16_OUT>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmD, const GemmParams p) {
   using Cfg = GemmCfg;
   constexpr int STAGES = Cfg::STAGES;
   constexpr int BN = Cfg::BN;
   extern __shared__ uint8_t gsm_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(gsm_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = gsm_raw + ((1024u - (ptx::smem_u32(gsm_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sf_full = drain + 1;  // [STAGES]: the stage's scales are in TMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + STAGES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
+      ptx::mbar_init(&sf_full[s], 4);
     }
     ptx::mbar_init(tfull, 1);
     ptx::mbar_init(tempty, 4);
@@ -226,7 +237,8 @@ __global__ void __launch_bounds__(192, 1)
         ptx::tc_fence_after();
         bool ok = true;
         for (int kt = kt0; kt < kt1; ++kt) {
-          if (!ptx::mbar_wait(&full[stage], phase, kWaitLimit)) {
+          // the scale warps saw the stage land (full) before writing its scales
+          if (!ptx::mbar_wait(&sf_full[stage], phase, kWaitLimit)) {
             atomicExch(p.err, kErrMma);
             ok = false;
             break;
@@ -235,15 +247,6 @@ __global__ void __launch_bounds__(192, 1)
           const int ns = min(4, p.kc - 4 * kt);
           const uint32_t sfa_t = tmem + (uint32_t)(Cfg::SF_BASE + stage * Cfg::SF_STAGE_COLS);
           const uint32_t sfb_t = sfa_t + 16u;
-          const uint32_t sfa_s = ptx::smem_u32(smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES);
-          const uint32_t sfb_s = ptx::smem_u32(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES);
-          for (int g = 0; g < ns; ++g) {
-            ptx::tc_cp_32x128b_warpx4(sfa_t + 4u * g, ptx::smem_desc(sfa_s + 512u * g, 16u, 128u, ptx::kSwizzleNone));
-#pragma unroll
-            for (int h = 0; h < BN / 128; ++h)
-              ptx::tc_cp_32x128b_warpx4(sfb_t + (uint32_t)(Cfg::SFB_COLS_PER_STEP * g + 4 * h),
-                                        ptx::smem_desc(sfb_s + 2048u * h + 512u * g, 16u, 128u, ptx::kSwizzleNone));
-          }
           const uint32_t a_s = ptx::smem_u32(smem + Cfg::OFF_A + stage * Cfg::A_BYTES);
           const uint32_t b_s = ptx::smem_u32(smem + Cfg::OFF_B + stage * Cfg::B_BYTES);
           for (int g = 0; g < ns; ++g) {
@@ -268,10 +271,60 @@ __global__ void __launch_bounds__(192, 1)
         if (!ptx::mbar_wait(drain, 0, kWaitLimit)) atomicExch(p.err, kErrDrain);
       }
     }
+  } else if (warp >= 6) {
+    // scale feed: every lane quarter q = warp % 4 gets the same words: lane
+    // 32 q + i, columns 4 g .. 4 g + 3 (A chunk g) and 16 + 8 g + 4 h .. +3
+    // (B half h, chunk g) = row i of that 512-byte SMEM atom, whose word j
+    // holds the 4 block scales of row i + 32 j.
+    const int q = warp & 3;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+      int mt, nt, kt0, kt1;
+      decode(tile, mt, nt, kt0, kt1);
+      for (int kt = kt0; kt < kt1; ++kt) {
+        if (!ptx::mbar_wait(&full[stage], phase, kWaitLimit)) {
+          if (lane == 0) atomicExch(p.err, kErrScaleFeed);
+          goto done;
+        }
+        const uint8_t* sa = smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES + 16 * lane;
+        const uint8_t* sb = smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES + 16 * lane;
+        uint32_t ra[16], rb[32];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          const uint4 v = *reinterpret_cast<const uint4*>(sa + 512 * g);
+          ra[4 * g] = v.x;
+          ra[4 * g + 1] = v.y;
+          ra[4 * g + 2] = v.z;
+          ra[4 * g + 3] = v.w;
+        }
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+          for (int g = 0; g < 4; ++g) {
+            const uint4 v = *reinterpret_cast<const uint4*>(sb + 2048 * h + 512 * g);
+            rb[8 * g + 4 * h] = v.x;
+            rb[8 * g + 4 * h + 1] = v.y;
+            rb[8 * g + 4 * h + 2] = v.z;
+            rb[8 * g + 4 * h + 3] = v.w;
+          }
+        const uint32_t t = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(Cfg::SF_BASE + stage * Cfg::SF_STAGE_COLS);
+        ptx::tmem_st16(t, ra);
+        ptx::tmem_st32(t + 16u, rb);
+        ptx::tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&sf_full[stage]);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
   } else {
     // epilogue warps: TMEM lane quarter (warp % 4) holds tile rows 32*(warp%4) .. +31
     const int q = warp & 3;
-    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps
+    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps (2-5)
     const float alpha = __ldg(p.ts_a) * __ldg(p.ts_b);
     const bool has_add = p.col_add != nullptr;
     const bool has_outer = p.row_vec != nullptr;

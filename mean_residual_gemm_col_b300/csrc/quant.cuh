@@ -248,8 +248,10 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
       c2[w] = sub2(sub2(tt, s2[w]), y);
       s2[w] = tt;
     };
-    // 8 rows (stride 32) at a time: pairwise sums, then one compensated add
-    auto group = [&](const uint4 (&v)[8]) {
+    // 8 rows (stride 32) at a time: pairwise sums, then one compensated add.
+    // nv < 8: only the first nv rows count (the others repeat a counted row,
+    // harmless for max / min, and are left out of the sum)
+    auto group = [&](const uint4 (&v)[8], int nv) {
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
         uint32_t x[8];
@@ -257,6 +259,9 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
         for (int j = 0; j < 8; ++j) x[j] = w == 0 ? v[j].x : w == 1 ? v[j].y : w == 2 ? v[j].z : v[j].w;
         mx2[w] = bmax2(mx2[w], bmax2(bmax2(bmax2(x[0], x[1]), bmax2(x[2], x[3])), bmax2(bmax2(x[4], x[5]), bmax2(x[6], x[7]))));
         mn2[w] = bmin2(mn2[w], bmin2(bmin2(bmin2(x[0], x[1]), bmin2(x[2], x[3])), bmin2(bmin2(x[4], x[5]), bmin2(x[6], x[7]))));
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+          if (j >= nv) x[j] = 0u;  // +0 + +0: adds nothing
         const uint64_t t = add2(add2(add2(bf2_to_f2(x[0]), bf2_to_f2(x[1])), add2(bf2_to_f2(x[2]), bf2_to_f2(x[3]))),
                                 add2(add2(bf2_to_f2(x[4]), bf2_to_f2(x[5])), add2(bf2_to_f2(x[6]), bf2_to_f2(x[7]))));
         kahan(w, t);
@@ -265,31 +270,28 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
     if (c0 < p.C) {
       const __nv_bfloat16* base = p.x + c0 + (rb0 + rl) * p.C;
       const int64_t nrow = rb1 > rb0 + rl ? (rb1 - rb0 - rl + 31) / 32 : 0;  // this thread's rows
-      const int64_t ng = nrow / 8;
+      const int64_t ng = (nrow + 7) / 8;                                      // groups, the last maybe partial
       const int64_t step = 32 * p.C;
       auto load = [&](uint4 (&v)[8], int64_t g) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = __ldg(reinterpret_cast<const uint4*>(base + (8 * g + j) * step));
+        for (int j = 0; j < 8; ++j)
+          v[j] = __ldg(reinterpret_cast<const uint4*>(base + min(8 * g + j, nrow - 1) * step));
+      };
+      auto run = [&](const uint4 (&v)[8], int64_t g) {
+        if (8 * g + 8 <= nrow)
+          group(v, 8);
+        else
+          group(v, (int)(nrow - 8 * g));
       };
       // two register buffers: the next group's loads are in flight while one is summed
       uint4 va[8], vb[8];
       if (ng > 0) load(va, 0);
       for (int64_t g = 0; g < ng; g += 2) {
         if (g + 1 < ng) load(vb, g + 1);
-        group(va);
+        run(va, g);
         if (g + 1 >= ng) break;
         if (g + 2 < ng) load(va, g + 2);
-        group(vb);
-      }
-      for (int64_t i = 8 * ng; i < nrow; ++i) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(base + i * step));
-        const uint32_t x[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int w = 0; w < 4; ++w) {
-          mx2[w] = bmax2(mx2[w], x[w]);
-          mn2[w] = bmin2(mn2[w], x[w]);
-          kahan(w, bf2_to_f2(x[w]));
-        }
+        run(vb, g + 1);
       }
     }
     // combine the 4 row lanes of this warp that share the columns (lanes differ by 8, 16)
@@ -579,6 +581,7 @@ constexpr int kQTile = 128;
 constexpr int kQThreads = 256;
 constexpr int kQWarps = kQThreads / 32;
 constexpr int kQBufs = 3;                         // tile buffers per CTA
+constexpr int kQCtasPerSm = 2;                    // resident CTAs per SM (registers, SMEM)
 constexpr int kQHalf = kQTile * 64 * 2;          // one 128-row x 64-column bf16 box (16 KB)
 constexpr int kQTileBytes = 2 * kQHalf;           // 32 KB
 // SMEM: tile buffers | mu [kQBufs][128] | inverse-scale tables [2][128] |
@@ -756,10 +759,10 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
 // rotated residual's per-layout maximum magnitude (Hadamard variant)
 // instead of quantizing.
 template <bool AMAX_ONLY>
-__global__ void __launch_bounds__(kQThreads, 2)
+__global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     split_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
   extern __shared__ uint8_t qraw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(qraw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sm = qraw + ((1024u - (ptx::smem_u32(qraw) & 1023u)) & 1023u);  // stays a shared-space pointer
   float* mu_s = reinterpret_cast<float*>(sm + kQOffMu);
   float* inv_s = reinterpret_cast<float*>(sm + kQOffInv);
   uint64_t* full = reinterpret_cast<uint64_t*>(sm + kQOffBar);
