@@ -20,20 +20,22 @@
 //              128x256x64 accumulating in TMEM; tcgen05.commit frees the
 //              stage and, after the last K tile, hands the accumulator to
 //              the epilogue.
-//   warps 6-9  scale feed: each writes a whole stage's block scales into
+//   warps 2-9  epilogue, two per TMEM lane quarter (warp % 4), each
+//              draining half of the accumulator columns: tcgen05.ld 32
+//              columns at a time, alpha scaling and the rank-one terms in
+//              binary32 (vector entries staged once per tile in SMEM and read
+//              as broadcasts), SMEM staging (128-byte swizzle), TMA tensor
+//              stores (which clip ragged edges).
+//   warps 10-13 scale feed: each writes a whole stage's block scales into
 //              its TMEM lane quarter with two tcgen05.st (registers -> TMEM),
 //              the same words a 32x128b.warpx4 copy of each SMEM scale atom
 //              would place there (lane 32 w + i, columns base_g .. +3 = atom
 //              row i).  This keeps the tensor pipe free of the 12 SMEM->TMEM
 //              copies per stage that would otherwise issue between the MMAs
 //              (each costs about as much tensor-pipe time as an MMA).
-//   warps 2-5  epilogue: tcgen05.ld 32 columns at a time, alpha scaling and
-//              the rank-one terms in binary32 (vector entries fetched once
-//              per 32 columns and broadcast by warp shuffles), SMEM staging
-//              (128-byte swizzle), TMA tensor stores (which clip ragged edges).
 // One 256-column accumulator leaves TMEM room for the scale stages.  With a
-// bf16 output the epilogue moves the whole accumulator into registers
-// (packed bf16) and releases TMEM before storing, so the next tile's MMAs
+// bf16 output the epilogue moves the accumulator into registers (packed
+// bf16) and releases TMEM before storing, so the next tile's MMAs
 // overlap the stores.  Every wait is bounded; on timeout the kernel sets the
 // error word, drains its own tensor-core work and frees its TMEM.  Launched
 // with programmatic dependent launch: set-up runs before the wait for the
@@ -78,8 +80,11 @@ struct GemmCfg {
   static constexpr int B_BYTES = BN * BKB;
   static constexpr int SFA_BYTES = 4 * 512;
   static constexpr int SFB_BYTES = (BN / 128) * 4 * 512;
+  static constexpr int EPI_WARPS = 8;             // 2 per TMEM lane quarter, each half of the columns
+  static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // accumulator columns per epilogue warp
+  static constexpr int EPI_NBUF = EPI_WARPS == 4 ? 2 : 1;  // staging boxes per epilogue warp
   static constexpr int EPI_BUF = 32 * 128;        // one warp's 32 rows x 128 bytes
-  static constexpr int EPI_BYTES = 4 * 2 * EPI_BUF;
+  static constexpr int EPI_BYTES = EPI_WARPS * EPI_NBUF * EPI_BUF;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -121,9 +126,12 @@ __device__ __forceinline__ void epi_math(float (&f)[32], const float (&acc)[32],
 }
 
 // Named barrier of the four epilogue warps (ids 1 and up are free for this).
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, %0;" ::"n"(32 * GemmCfg::EPI_WARPS) : "memory");
+}
 
-constexpr int kGemmThreads = 320;  // producer, MMA, 4 epilogue warps, 4 scale-feed warps
+// warps: producer, MMA issuer, GemmCfg::EPI_WARPS epilogue warps, 4 scale-feed warps
+constexpr int kGemmThreads = 32 * (2 + GemmCfg::EPI_WARPS + 4);
 
 template <bool BF16_OUT>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -150,7 +158,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ptx::mbar_init(&sf_full[s], 4);
     }
     ptx::mbar_init(tfull, 1);
-    ptx::mbar_init(tempty, 4);
+    ptx::mbar_init(tempty, Cfg::EPI_WARPS);
     ptx::mbar_init(drain, 1);
     ptx::fence_mbar_init();
   }
@@ -271,7 +279,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         if (!ptx::mbar_wait(drain, 0, kWaitLimit)) atomicExch(p.err, kErrDrain);
       }
     }
-  } else if (warp >= 6) {
+  } else if (warp >= 2 + Cfg::EPI_WARPS) {
     // scale feed: every lane quarter q = warp % 4 gets the same words: lane
     // 32 q + i, columns 4 g .. 4 g + 3 (A chunk g) and 16 + 8 g + 4 h .. +3
     // (B half h, chunk g) = row i of that 512-byte SMEM atom, whose word j
@@ -322,13 +330,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       }
     }
   } else {
-    // epilogue warps: TMEM lane quarter (warp % 4) holds tile rows 32*(warp%4) .. +31
+    // epilogue warps: TMEM lane quarter (warp % 4) holds tile rows 32*(warp%4) .. +31;
+    // warp 2 + 4 k + .. drains accumulator columns EPI_COLS * k .. +EPI_COLS - 1
     const int q = warp & 3;
-    const int et = threadIdx.x - 64;  // 0..127 over the epilogue warps (2-5)
+    const int cb = Cfg::EPI_COLS * ((warp - 2) >> 2);  // this warp's first column
+    const int et = threadIdx.x - 64;  // 0 .. 32 EPI_WARPS - 1 over the epilogue warps
     const float alpha = __ldg(p.ts_a) * __ldg(p.ts_b);
     const bool has_add = p.col_add != nullptr;
     const bool has_outer = p.row_vec != nullptr;
-    uint8_t* stage_base = smem + Cfg::OFF_EPI + q * 2 * Cfg::EPI_BUF;
+    uint8_t* stage_base = smem + Cfg::OFF_EPI + (warp - 2) * Cfg::EPI_NBUF * Cfg::EPI_BUF;
     float* vec_base = reinterpret_cast<float*>(smem + Cfg::OFF_VEC);
     __shared__ int s_ok[2];
     int sbuf = 0;
@@ -343,13 +353,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // reaches the next tile's writes only after every warp passed this barrier)
       float* cadd_s = vec_base + (it & 1) * 2 * BN;
       float* cvec_s = cadd_s + BN;
-      for (int c = et; c < BN; c += 128) {
+      for (int c = et; c < BN; c += 32 * Cfg::EPI_WARPS) {
         const int col = nt * BN + c;
         cadd_s[c] = (has_add && col < p.N) ? __ldg(p.col_add + col) : 0.f;
         cvec_s[c] = (has_outer && col < p.N) ? __ldg(p.col_vec + col) : 0.f;
       }
       // one thread waits for the accumulator; the barrier hands its verdict (and
-      // the staged vectors) to all four warps, so they leave the loop together
+      // the staged vectors) to all epilogue warps, so they leave the loop together
       if (et == 0) s_ok[it & 1] = ptx::mbar_wait(tfull, it & 1, kWaitLimit) ? 1 : 0;
       epi_bar();
       if (!s_ok[it & 1]) {
@@ -362,7 +372,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       // stage one 32-row x 128-byte box in swizzled SMEM and store it with TMA
       auto store_box = [&](const uint4 (&w)[8], int col0) {
         uint8_t* sb = stage_base + sbuf * Cfg::EPI_BUF;
-        if (lane == 0) ptx::bulk_wait_read<1>();
+        if (lane == 0) ptx::bulk_wait_read<Cfg::EPI_NBUF - 1>();
         __syncwarp();
         uint8_t* srow = sb + lane * 128;
 #pragma unroll
@@ -373,7 +383,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ptx::tma_store_2d(&tmD, sb, col0, row0);
           ptx::bulk_commit();
         }
-        sbuf ^= 1;
+        sbuf = (sbuf + 1) % Cfg::EPI_NBUF;
       };
       auto store_f32 = [&](const float (&f)[32], int c) {
         uint4 w[8];
@@ -385,17 +395,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       };
 
       if (BF16_OUT) {
-        // whole accumulator -> packed bf16 registers, release TMEM, then store
-        uint32_t packed[BN / 2];
+        // this warp's accumulator columns -> packed bf16 registers, release TMEM, then store
+        uint32_t packed[Cfg::EPI_COLS / 2];
 #pragma unroll
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = 0; c < Cfg::EPI_COLS; c += 32) {
           uint32_t v[32];
-          ptx::tmem_ld32(t_row + (uint32_t)c, v);
+          ptx::tmem_ld32(t_row + (uint32_t)(cb + c), v);
           ptx::tmem_ld_wait();
           float acc[32], f[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) acc[j] = alpha * __uint_as_float(v[j]);
-          epi_math(f, acc, has_add, cadd_s + c, has_outer, rterm, cvec_s + c);
+          epi_math(f, acc, has_add, cadd_s + cb + c, has_outer, rterm, cvec_s + cb + c);
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * j], f[2 * j + 1]);
@@ -406,21 +416,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(tempty);
 #pragma unroll
-        for (int c = 0; c < BN; c += 64) {
+        for (int c = 0; c < Cfg::EPI_COLS; c += 64) {
           uint4 w[8];
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             w[k] = make_uint4(packed[c / 2 + 4 * k], packed[c / 2 + 4 * k + 1], packed[c / 2 + 4 * k + 2],
                               packed[c / 2 + 4 * k + 3]);
-          store_box(w, nt * BN + c);
+          store_box(w, nt * BN + cb + c);
         }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < BN; c += 32) {
+        for (int c = cb; c < cb + Cfg::EPI_COLS; c += 32) {
           uint32_t v[32];
           ptx::tmem_ld32(t_row + (uint32_t)c, v);
           ptx::tmem_ld_wait();
-          if (c + 32 == BN) {
+          if (c + 32 == cb + Cfg::EPI_COLS) {
             // last chunk is in registers: the accumulator may be overwritten
             ptx::tc_fence_before();
             __syncwarp();
