@@ -75,8 +75,12 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(cuda_lib):
     lib = cuda_lib
     cap = 8 << 20
     rows, cols = 64, 1024
-    while lib.averis_quantize_workspace_bytes(rows, cols, 1) <= cap:
+    for _ in range(40):                  # bounded: the need grows with the column count
+        if lib.averis_quantize_workspace_bytes(rows, cols, 1) > cap:
+            break
         cols *= 2
+    else:
+        pytest.skip("the quantize workspace never exceeds the no-alloc scratch")
     fake = ctypes.c_void_p(256)          # never dereferenced: the size check comes first
     nv_row = capi.NVFP4Struct(256, 256, 256, rows, cols)
     st = lib.averis_quantize_noalloc(fake, rows, cols, 0, None, None, None, ctypes.byref(nv_row), None, None)
