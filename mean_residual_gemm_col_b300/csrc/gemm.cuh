@@ -297,8 +297,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         }
         const uint8_t* sa = smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES + 16 * lane;
         const uint8_t* sb = smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES + 16 * lane;
-        constexpr int NH = BN / 128;  // 128-row halves of B
-        uint32_t ra[16], rb[16 * NH];
+        uint32_t ra[16], rb[32];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           const uint4 v = *reinterpret_cast<const uint4*>(sa + 512 * g);
@@ -308,21 +307,18 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           ra[4 * g + 3] = v.w;
         }
 #pragma unroll
-        for (int h = 0; h < NH; ++h)
+        for (int h = 0; h < 2; ++h)
 #pragma unroll
           for (int g = 0; g < 4; ++g) {
             const uint4 v = *reinterpret_cast<const uint4*>(sb + 2048 * h + 512 * g);
-            rb[4 * NH * g + 4 * h] = v.x;
-            rb[4 * NH * g + 4 * h + 1] = v.y;
-            rb[4 * NH * g + 4 * h + 2] = v.z;
-            rb[4 * NH * g + 4 * h + 3] = v.w;
+            rb[8 * g + 4 * h] = v.x;
+            rb[8 * g + 4 * h + 1] = v.y;
+            rb[8 * g + 4 * h + 2] = v.z;
+            rb[8 * g + 4 * h + 3] = v.w;
           }
         const uint32_t t = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(Cfg::SF_BASE + stage * Cfg::SF_STAGE_COLS);
         ptx::tmem_st16(t, ra);
-        if constexpr (NH == 2)
-          ptx::tmem_st32(t + 16u, *reinterpret_cast<const uint32_t(*)[32]>(rb));
-        else
-          ptx::tmem_st16(t + 16u, *reinterpret_cast<const uint32_t(*)[16]>(rb));
+        ptx::tmem_st32(t + 16u, rb);
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
