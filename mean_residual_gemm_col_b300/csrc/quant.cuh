@@ -80,6 +80,31 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
   return d;
 }
 
+// fl32(bf16 - binary32) for both halves of a packed bf16 word (mixed-precision subtract; the
+// bf16 operand converts exactly, so this is the binary32 subtraction of the widened value).
+__device__ __forceinline__ uint64_t bf2_sub_f2(uint32_t w, uint64_t m) {
+  float d0, d1;
+  asm("{\n .reg .b16 l, h;\n .reg .f32 m0, m1;\n mov.b32 {l, h}, %2;\n mov.b64 {m0, m1}, %3;\n"
+      " sub.rn.f32.bf16 %0, l, m0;\n sub.rn.f32.bf16 %1, h, m1;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "r"(w), "l"(m));
+  return f2pack(d0, d1);
+}
+// fl32(bf16 - m) of one half (hi: the upper one) of each of two words.
+__device__ __forceinline__ uint64_t bf_pair_sub(uint32_t wa, uint32_t wb, bool hi, float m) {
+  float d0, d1;
+  if (hi)
+    asm("{\n .reg .b16 l0, h0, l1, h1;\n mov.b32 {l0, h0}, %2;\n mov.b32 {l1, h1}, %3;\n"
+        " sub.rn.f32.bf16 %0, h0, %4;\n sub.rn.f32.bf16 %1, h1, %4;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(wa), "r"(wb), "f"(m));
+  else
+    asm("{\n .reg .b16 l0, h0, l1, h1;\n mov.b32 {l0, h0}, %2;\n mov.b32 {l1, h1}, %3;\n"
+        " sub.rn.f32.bf16 %0, l0, %4;\n sub.rn.f32.bf16 %1, l1, %4;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(wa), "r"(wb), "f"(m));
+  return f2pack(d0, d1);
+}
 // The two bf16 values of a packed word as a binary32 pair (exact).
 __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return f2pack(bf16lo(w), bf16hi(w)); }
 // Element-wise max / min of two packed bf16 pairs (exact).
@@ -683,7 +708,7 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
       float rx[16];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        const uint64_t d = sub2(bf2_to_f2(wv[e]), m2[e]);
+        const uint64_t d = bf2_sub_f2(wv[e], m2[e]);
         rx[2 * e] = f2lo(d);
         rx[2 * e + 1] = f2hi(d);
       }
@@ -717,13 +742,12 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
     const int64_t off = (r0 + row0) / 2;  // code byte offset of the block within a column
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const uint64_t mm = f2pack(mc[j], mc[j]);
       float rx[16];
 #pragma unroll
       for (int e = 0; e < 16; e += 2) {
         const uint32_t wa = (j >> 1) ? x[e].y : x[e].x;
         const uint32_t wb = (j >> 1) ? x[e + 1].y : x[e + 1].x;
-        const uint64_t d = sub2(f2pack((j & 1) ? bf16hi(wa) : bf16lo(wa), (j & 1) ? bf16hi(wb) : bf16lo(wb)), mm);
+        const uint64_t d = bf_pair_sub(wa, wb, (j & 1) != 0, mc[j]);
         rx[e] = f2lo(d);
         rx[e + 1] = f2hi(d);
       }
