@@ -111,18 +111,60 @@ def max_over_ranks(v, ws):
 # ----------------------------------------------------------------- clocks --
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons while the timed region runs."""
+    """SM clock, power and throttle reasons sampled while the timed region runs.
+
+    NVML read-only queries every 10 ms on a thread (so a sub-second timed
+    region still gets tens of samples); nvidia-smi at 200 ms if NVML is not
+    available.  Only samples taken between __enter__ and __exit__ count.
+    """
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, device_index):
         self.dev = device_index
+        self.rows = []       # (sm_mhz, max_mhz, power_w, set of active reason names)
         self.proc = None
         self.path = None
+        self.thread = None
+        self.stop = None
+
+    def _nvml_handle(self):
+        import pynvml
+
+        pynvml.nvmlInit()
+        n = pynvml.nvmlDeviceGetCount()
+        return pynvml, pynvml.nvmlDeviceGetHandleByIndex(0 if n == 1 else self.dev)
+
+    def _poll(self, nv, h):
+        bits = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
+                "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
+                "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
+                "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
+        while not self.stop.is_set():
+            try:
+                r = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
+                self.rows.append((float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)),
+                                  float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)),
+                                  nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
+                                  {k for k, b in bits.items() if r & b}))
+            except Exception:
+                break
+            time.sleep(0.01)
 
     def __enter__(self):
+        import threading
+
+        try:
+            nv, h = self._nvml_handle()
+            self.stop = threading.Event()
+            self.thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
+            self.thread.start()
+            return self
+        except Exception:
+            self.thread = None
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -136,6 +178,10 @@ class ClockSampler:
         return self
 
     def __exit__(self, *exc):
+        if self.thread is not None:
+            self.stop.set()
+            self.thread.join(timeout=5)
+            return
         if self.proc is not None:
             self.proc.terminate()
             try:
@@ -143,32 +189,30 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
         self.out.close()
-
-    def summary(self):
-        rows = []
         if self.path and os.path.exists(self.path):
+            def num(v):
+                try:
+                    return float(v)
+                except ValueError:
+                    return None
             with open(self.path) as f:
                 for ln in f:
-                    p = [s.strip() for s in ln.split(",")]
-                    if len(p) >= 9:
-                        rows.append(p)
+                    p = [v.strip() for v in ln.split(",")]
+                    if len(p) >= 9 and num(p[1]) is not None:
+                        self.rows.append((num(p[1]), num(p[2]), num(p[3]),
+                                          {self.NAMES[i] for i in range(4) if p[5 + i].lower().startswith("active")}))
             os.unlink(self.path)
-        if not rows:
+
+    def summary(self):
+        if not self.rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-
-        def num(s):
-            try:
-                return float(s)
-            except ValueError:
-                return None
-
-        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
-        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
-        pw = [num(r[3]) for r in rows if num(r[3]) is not None]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(rows)}
+        sm = [r[0] for r in self.rows]
+        mx = [r[1] for r in self.rows if r[1] is not None]
+        pw = [r[2] for r in self.rows if r[2] is not None]
+        reasons = sorted(set().union(*(r[3] for r in self.rows)))
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(self.rows),
+                "source": "nvml 10 ms" if self.thread is not None else "nvidia-smi 200 ms"}
 
 
 # ----------------------------------------------------------- GPU workload --
