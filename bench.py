@@ -130,6 +130,7 @@ class ClockSampler:
         self.path = None
         self.thread = None
         self.stop = None
+        self.nvml_error = None
 
     def _nvml_handle(self):
         import pynvml
@@ -163,8 +164,9 @@ class ClockSampler:
             self.thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
             self.thread.start()
             return self
-        except Exception:
+        except Exception as e:  # no NVML: fall back to nvidia-smi
             self.thread = None
+            self.nvml_error = f"{type(e).__name__}: {e}"[:120]
         fd, self.path = tempfile.mkstemp(suffix=".csv")
         os.close(fd)
         try:
@@ -210,9 +212,12 @@ class ClockSampler:
         mx = [r[1] for r in self.rows if r[1] is not None]
         pw = [r[2] for r in self.rows if r[2] is not None]
         reasons = sorted(set().union(*(r[3] for r in self.rows)))
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
-                "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(self.rows),
-                "source": "nvml 10 ms" if self.thread is not None else "nvidia-smi 200 ms"}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+               "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(self.rows),
+               "source": "nvml 10 ms" if self.thread is not None else "nvidia-smi 200 ms"}
+        if self.nvml_error:
+            out["nvml_error"] = self.nvml_error
+        return out
 
 
 # ----------------------------------------------------------- GPU workload --
