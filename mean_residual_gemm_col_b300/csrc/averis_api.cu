@@ -81,10 +81,15 @@ averis_status device_info(DeviceInfo** out) {
 }
 
 averis_status set_attrs() {
-  if (cudaFuncSetAttribute(split_quant_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+  if (cudaFuncSetAttribute(colstats_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatsSmem) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(split_quant_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(split_quant_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+  if (cudaFuncSetAttribute(split_quant_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+      cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(split_quant_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return AVERIS_ERR_CUDA;
   if (cudaFuncSetAttribute(gemm_nvfp4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM) !=
@@ -202,7 +207,8 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   sp.split = split ? 1 : 0;
   sp.hadamard = had ? 1 : 0;
   sp.mu = mu;
-  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), 0, s, sp) != cudaSuccess) return AVERIS_ERR_CUDA;
+  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), kStatsSmem, s, sp) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
 
   // The quantize pass also writes the NVFP4 mean (one of its CTAs) and resets
   // the control block, so it runs even with no residual layout requested.
@@ -271,12 +277,13 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   if (had) {
     QuantParams ap = qp;  // rotated-maximum pass: tiles only
     ap.mean_ctas = 0;
-    if (launch_pdl(split_quant_kernel<true>, dim3(std::max(1, tile_ctas)), dim3(kQThreads), kQSmem, s, tx, ap) !=
+    if (launch_pdl(split_quant_kernel<true, true>, dim3(std::max(1, tile_ctas)), dim3(kQThreads), kQSmem, s, tx, ap) !=
         cudaSuccess)
       return AVERIS_ERR_CUDA;
   }
-  if (launch_pdl(split_quant_kernel<false>, dim3(std::max(1, qp.mean_ctas + tile_ctas)), dim3(kQThreads), kQSmem, s,
-                 tx, qp) != cudaSuccess)
+  // the rotation is a template parameter: the plain kernel carries no butterfly code
+  auto* qk = had ? split_quant_kernel<false, true> : split_quant_kernel<false, false>;
+  if (launch_pdl(qk, dim3(std::max(1, qp.mean_ctas + tile_ctas)), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }

@@ -242,7 +242,11 @@ struct StatsParams {
 // which CTA is last -- giving mu_j = fl32(S_j / R) and the residual's exact
 // maximum magnitude max(|fl32(max_j - mu_j)|, |fl32(min_j - mu_j)|) (binary32
 // subtraction is monotone), folded into the control block with atomicMax.
+constexpr int kStatsGroups = 3;                              // 8-row groups in flight per thread
+constexpr int kStatsSmem = kStatsGroups * 8 * 256 * 16;       // cp.async ring (96 KB)
+
 __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
+  extern __shared__ __align__(16) uint8_t stats_ring[];
   __shared__ F2 s_sum[8][64];
   __shared__ float s_mx[8][64], s_mn[8][64];
   __shared__ float red[8];
@@ -297,27 +301,39 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
       const int64_t nrow = rb1 > rb0 + rl ? (rb1 - rb0 - rl + 31) / 32 : 0;  // this thread's rows
       const int64_t ng = (nrow + 7) / 8;                                      // groups, the last maybe partial
       const int64_t step = 32 * p.C;
-      auto load = [&](uint4 (&v)[8], int64_t g) {
+      // SMEM ring of kStatsGroups groups of 8 rows per thread, filled by
+      // cp.async (16 bytes per row): the copies of the next groups stay in
+      // flight without holding registers.  Each thread reads only its own
+      // slots, so no barrier is needed.  Rows past this thread's last repeat
+      // the last row (harmless for max / min; group() leaves them out of the sum).
+      uint4* ring = reinterpret_cast<uint4*>(stats_ring) + threadIdx.x;
+      auto issue = [&](int64_t g) {
+        uint4* slot = ring + (int)(g % kStatsGroups) * 8 * 256;
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          v[j] = __ldg(reinterpret_cast<const uint4*>(base + min(8 * g + j, nrow - 1) * step));
+          ptx::cp_async16(slot + 256 * j, base + min(8 * g + j, nrow - 1) * step, 16u);
+        ptx::cp_async_commit();
       };
-      auto run = [&](const uint4 (&v)[8], int64_t g) {
+#pragma unroll 1
+      for (int64_t g = 0; g < kStatsGroups; ++g) {
+        if (g < ng) issue(g);
+        else ptx::cp_async_commit();  // empty group: the wait count below stays uniform
+      }
+#pragma unroll 1
+      for (int64_t g = 0; g < ng; ++g) {
+        ptx::cp_async_wait<kStatsGroups - 1>();  // group g has landed
+        const uint4* slot = ring + (int)(g % kStatsGroups) * 8 * 256;
+        uint4 v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = slot[256 * j];
         if (8 * g + 8 <= nrow)
           group(v, 8);
         else
           group(v, (int)(nrow - 8 * g));
-      };
-      // two register buffers: the next group's loads are in flight while one is summed
-      uint4 va[8], vb[8];
-      if (ng > 0) load(va, 0);
-      for (int64_t g = 0; g < ng; g += 2) {
-        if (g + 1 < ng) load(vb, g + 1);
-        run(va, g);
-        if (g + 1 >= ng) break;
-        if (g + 2 < ng) load(va, g + 2);
-        run(vb, g + 1);
+        if (g + kStatsGroups < ng) issue(g + kStatsGroups);
+        else ptx::cp_async_commit();
       }
+      ptx::cp_async_wait<0>();
     }
     // combine the 4 row lanes of this warp that share the columns (lanes differ by 8, 16)
 #pragma unroll
@@ -678,7 +694,7 @@ __device__ __forceinline__ uint32_t quant16_tab(const float (&r)[16], float den,
 // Codes go to global memory directly; block scales to the SMEM staging of
 // this buffer (the tile fills exactly two 512-byte atoms of each layout).
 // EDGE: the tile crosses row R or column C (masked, zero-filled blocks).
-template <bool AMAX_ONLY, bool EDGE>
+template <bool AMAX_ONLY, bool HAD, bool EDGE>
 __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint8_t* buf, const float* mub,
                                                 uint8_t* stage, int64_t r0, int64_t c0, float den_row, float den_col,
                                                 bool pos_row, bool pos_col, const float* inv_s, bool rows_on,
@@ -717,7 +733,7 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
 #pragma unroll
         for (int e = 0; e < 16; ++e) rx[e] = 0.f;
       }
-      if (p.hadamard) fwht16(rx);
+      if (HAD) fwht16(rx);
       if (AMAX_ONLY) {
         amax_row = fmaxf(amax_row, absmax16(rx));
       } else {
@@ -758,7 +774,7 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
         for (int e = 0; e < 16; ++e)
           if (!cvalid || r0 + row0 + e >= p.R) rx[e] = 0.f;
       }
-      if (p.hadamard) fwht16(rx);
+      if (HAD) fwht16(rx);
       if (AMAX_ONLY) {
         amax_col = fmaxf(amax_col, absmax16(rx));
       } else {
@@ -782,7 +798,7 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
 // CTA to finish resets the control block's maxima.  AMAX_ONLY: compute the
 // rotated residual's per-layout maximum magnitude (Hadamard variant)
 // instead of quantizing.
-template <bool AMAX_ONLY>
+template <bool AMAX_ONLY, bool HAD>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     split_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
   extern __shared__ uint8_t qraw[];
@@ -873,10 +889,10 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     uint8_t* stage = sm + kQOffStage + b * kQStageBytes;
     const float* mub = mu_s + 128 * b;
     if (r0 + kQTile > p.R || c0 + kQTile > p.C)
-      quant_tile_warp<AMAX_ONLY, true>(p, buf, mub, stage, r0, c0, den_row, den_col, s_row > 0.f, s_col > 0.f, inv_s,
+      quant_tile_warp<AMAX_ONLY, HAD, true>(p, buf, mub, stage, r0, c0, den_row, den_col, s_row > 0.f, s_col > 0.f, inv_s,
                                        rows_on, cols_on, amax_row, amax_col);
     else
-      quant_tile_warp<AMAX_ONLY, false>(p, buf, mub, stage, r0, c0, den_row, den_col, s_row > 0.f, s_col > 0.f,
+      quant_tile_warp<AMAX_ONLY, HAD, false>(p, buf, mub, stage, r0, c0, den_row, den_col, s_row > 0.f, s_col > 0.f,
                                         inv_s, rows_on, cols_on, amax_row, amax_col);
     // count this warp done with the buffer; the last of the kQWarps writes the
     // staged scale atoms, then refills the buffer (its own reads are done too)
