@@ -147,8 +147,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 1;
   uint64_t* drain = tempty + 1;
-  uint64_t* sf_full = drain + 1;  // [STAGES]: the stage's scales are in TMEM
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_full + STAGES);
+  uint64_t* sf_full = drain + 1;            // [STAGES]: the stage's scales are in TMEM
+  uint64_t* sf_loaded = sf_full + STAGES;  // [STAGES]: the stage's scale atoms are in SMEM
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_loaded + STAGES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -156,6 +157,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       ptx::mbar_init(&full[s], 1);
       ptx::mbar_init(&empty[s], 1);
       ptx::mbar_init(&sf_full[s], 4);
+      ptx::mbar_init(&sf_loaded[s], 1);
     }
     ptx::mbar_init(tfull, 1);
     ptx::mbar_init(tempty, Cfg::EPI_WARPS);
@@ -209,19 +211,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             goto done;
           }
           const int ns = min(4, p.kc - 4 * kt);
-          const uint32_t bytes = Cfg::A_BYTES + Cfg::B_BYTES + (uint32_t)ns * 512u * (1u + (uint32_t)nsfb);
-          ptx::mbar_arrive_expect_tx(&full[stage], bytes);
-          ptx::tma_load_2d(smem + Cfg::OFF_A + stage * Cfg::A_BYTES, &tmA, kt * Cfg::BKB, mt * Cfg::BM, &full[stage]);
-          ptx::tma_load_2d(smem + Cfg::OFF_B + stage * Cfg::B_BYTES, &tmB, kt * Cfg::BKB, nt * BN, &full[stage]);
+          // the small scale atoms first, on their own barrier: the scale warps
+          // move them into TMEM while the operand tiles are still arriving
+          ptx::mbar_arrive_expect_tx(&sf_loaded[stage], (uint32_t)ns * 512u * (1u + (uint32_t)nsfb));
           ptx::bulk_load(smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES, p.sfa + ((int64_t)mt * p.kc + 4 * kt) * 512,
-                         ns * 512u, &full[stage]);
+                         ns * 512u, &sf_loaded[stage]);
 #pragma unroll
           for (int h = 0; h < BN / 128; ++h) {
             const int rb = nt * (BN / 128) + h;
             if (rb < p.rb_b)
               ptx::bulk_load(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES + h * 2048,
-                             p.sfb + ((int64_t)rb * p.kc + 4 * kt) * 512, ns * 512u, &full[stage]);
+                             p.sfb + ((int64_t)rb * p.kc + 4 * kt) * 512, ns * 512u, &sf_loaded[stage]);
           }
+          ptx::mbar_arrive_expect_tx(&full[stage], (uint32_t)(Cfg::A_BYTES + Cfg::B_BYTES));
+          ptx::tma_load_2d(smem + Cfg::OFF_A + stage * Cfg::A_BYTES, &tmA, kt * Cfg::BKB, mt * Cfg::BM, &full[stage]);
+          ptx::tma_load_2d(smem + Cfg::OFF_B + stage * Cfg::B_BYTES, &tmB, kt * Cfg::BKB, nt * BN, &full[stage]);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -245,8 +249,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         ptx::tc_fence_after();
         bool ok = true;
         for (int kt = kt0; kt < kt1; ++kt) {
-          // the scale warps saw the stage land (full) before writing its scales
-          if (!ptx::mbar_wait(&sf_full[stage], phase, kWaitLimit)) {
+          // operand tiles in SMEM, scales in TMEM
+          if (!ptx::mbar_wait(&full[stage], phase, kWaitLimit) || !ptx::mbar_wait(&sf_full[stage], phase, kWaitLimit)) {
             atomicExch(p.err, kErrMma);
             ok = false;
             break;
@@ -291,7 +295,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int mt, nt, kt0, kt1;
       decode(tile, mt, nt, kt0, kt1);
       for (int kt = kt0; kt < kt1; ++kt) {
-        if (!ptx::mbar_wait(&full[stage], phase, kWaitLimit)) {
+        if (!ptx::mbar_wait(&sf_loaded[stage], phase, kWaitLimit)) {
           if (lane == 0) atomicExch(p.err, kErrScaleFeed);
           goto done;
         }
