@@ -47,7 +47,7 @@ CPU_SAMPLE_TOKENS = 256
 # DRAM bytes (read + write) per GEMM launch of this step, averaged over the 12
 # GEMM launches of one ncu capture (profiles/dram_traffic_qwen3_step.md), valid
 # only for the GEMM source it was taken on.
-GEMM_TRAFFIC = {"7c504c4012a18912": 251.1e6 / 12}
+GEMM_TRAFFIC = {"c8581fbd97ab5c73": 250.9e6 / 12}
 
 
 def gemm_traffic_per_launch():
