@@ -158,6 +158,18 @@ bool nvfp4_ok(const averis_nvfp4* t, int64_t rows, int64_t cols) {
          aligned(t->tensor_scale, 4);
 }
 
+// 2-D tiled tensor map (128-byte swizzle, zero fill out of bounds).
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
+               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return g_encode(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // ------------------------------------------------------------- quantize --
 
 // Largest column count of a mean split: the NVFP4 mean is staged in the
@@ -207,7 +219,12 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   sp.split = split ? 1 : 0;
   sp.hadamard = had ? 1 : 0;
   sp.mu = mu;
-  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), kStatsSmem, s, sp) != cudaSuccess)
+  sp.err = dev->err_word;
+  CUtensorMap tstats;  // X in boxes of 64 columns x 256 rows for the stats pass
+  if (!encode_2d(&tstats, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x), (uint64_t)C, (uint64_t)R,
+                 (uint64_t)C * 2, 64u, (uint32_t)kStatsBoxRows))
+    return AVERIS_ERR_CUDA;
+  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
     return AVERIS_ERR_CUDA;
 
   // The quantize pass also writes the NVFP4 mean (one of its CTAs) and resets
@@ -290,16 +307,6 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
 
 // ----------------------------------------------------------------- GEMM --
 
-bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, void* base, uint64_t inner, uint64_t rows,
-               uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
-  const cuuint64_t dims[2] = {inner, rows};
-  const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {box_inner, box_rows};
-  const cuuint32_t estr[2] = {1, 1};
-  return g_encode(map, dt, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 // early_start: the kernel launched just before this GEMM produced none of its
 // inputs (see GemmParams::early_start).

@@ -220,10 +220,11 @@ __device__ __forceinline__ float e2m1_val(uint32_t c4) {
 struct StatsParams {
   const __nv_bfloat16* x;
   int64_t R, C;
-  int64_t rows_per;   // rows per CTA row block (multiple of 256)
+  int64_t rows_per;   // rows per CTA row block (multiple of 32)
   int nstrips;        // ceil(C / 64) column strips of 64
   ColPartial* part;   // [gridDim.y][C] per-row-block partials
   unsigned* ctrl;
+  int* err;           // device error word (a box that never arrived)
   int split;          // mean split on
   int hadamard;       // rotation on (the rotated residual's maximum comes from the amax pass)
   float* mu;          // [C] out (split)
@@ -242,16 +243,28 @@ struct StatsParams {
 // which CTA is last -- giving mu_j = fl32(S_j / R) and the residual's exact
 // maximum magnitude max(|fl32(max_j - mu_j)|, |fl32(min_j - mu_j)|) (binary32
 // subtraction is monotone), folded into the control block with atomicMax.
-constexpr int kStatsGroups = 3;                              // 8-row groups in flight per thread
-constexpr int kStatsSmem = kStatsGroups * 8 * 256 * 16;       // cp.async ring (96 KB)
+constexpr int kStatsBoxRows = 256;                           // rows per TMA box (8 per thread)
+constexpr int kStatsBufs = 3;                                 // boxes in flight per CTA
+constexpr int kStatsBox = kStatsBoxRows * 128;                // 64 bf16 columns x 256 rows (32 KB)
+constexpr int kStatsSmem = kStatsBufs * kStatsBox + 1024;     // + alignment slack for the 128-byte swizzle
 
-__global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
-  extern __shared__ __align__(16) uint8_t stats_ring[];
+__global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant__ CUtensorMap tmX, StatsParams p) {
+  extern __shared__ uint8_t stats_raw[];
+  uint8_t* ring = stats_raw + ((1024u - (ptx::smem_u32(stats_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
   __shared__ F2 s_sum[8][64];
   __shared__ float s_mx[8][64], s_mn[8][64];
   __shared__ float red[8];
   __shared__ int s_last;
+  __shared__ uint64_t s_full[kStatsBufs];
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < kStatsBufs; ++b) ptx::mbar_init(&s_full[b], 1);
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmX);
+  }
+  __syncthreads();
   ptx::pdl_wait_and_release();
+  uint32_t it = 0;  // boxes consumed by this CTA (buffer it % kStatsBufs, phase it / kStatsBufs)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = tid & 7;     // 8-column group inside the strip
@@ -260,7 +273,6 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
   const int64_t rb1 = min(p.R, rb0 + p.rows_per);
 
   for (int strip = blockIdx.x; strip < p.nstrips; strip += gridDim.x) {
-    const int64_t c0 = (int64_t)strip * 64 + 8 * g8;
     // column pairs (2w, 2w+1): Kahan-compensated binary32 sums, packed bf16 max / min
     uint64_t s2[4], c2[4];
     uint32_t mx2[4], mn2[4];
@@ -296,44 +308,50 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(StatsParams p) {
         kahan(w, t);
       }
     };
-    if (c0 < p.C) {
-      const __nv_bfloat16* base = p.x + c0 + (rb0 + rl) * p.C;
-      const int64_t nrow = rb1 > rb0 + rl ? (rb1 - rb0 - rl + 31) / 32 : 0;  // this thread's rows
-      const int64_t ng = (nrow + 7) / 8;                                      // groups, the last maybe partial
-      const int64_t step = 32 * p.C;
-      // SMEM ring of kStatsGroups groups of 8 rows per thread, filled by
-      // cp.async (16 bytes per row): the copies of the next groups stay in
-      // flight without holding registers.  Each thread reads only its own
-      // slots, so no barrier is needed.  Rows past this thread's last repeat
-      // the last row (harmless for max / min; group() leaves them out of the sum).
-      uint4* ring = reinterpret_cast<uint4*>(stats_ring) + threadIdx.x;
-      auto issue = [&](int64_t g) {
-        uint4* slot = ring + (int)(g % kStatsGroups) * 8 * 256;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          ptx::cp_async16(slot + 256 * j, base + min(8 * g + j, nrow - 1) * step, 16u);
-        ptx::cp_async_commit();
-      };
-#pragma unroll 1
-      for (int64_t g = 0; g < kStatsGroups; ++g) {
-        if (g < ng) issue(g);
-        else ptx::cp_async_commit();  // empty group: the wait count below stays uniform
+    // the strip's rows arrive by TMA in boxes of 256 rows x 64 columns (128-byte
+    // swizzle: 16-byte chunk j of box row r at chunk j ^ (r % 8)); thread rows
+    // rl, rl + 32, ... of a box are one 8-row group.  Rows past this CTA's block
+    // are left out (max / min see a repeat of a counted row, the sum zeros).
+    const int64_t nbox = (rb1 - rb0 + kStatsBoxRows - 1) / kStatsBoxRows;
+    if (threadIdx.x == 0)
+      for (int64_t k = 0; k < kStatsBufs && k < nbox; ++k) {
+        const uint32_t b = (it + (uint32_t)k) % kStatsBufs;
+        ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
+        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64, (int32_t)(rb0 + k * kStatsBoxRows), &s_full[b]);
       }
-#pragma unroll 1
-      for (int64_t g = 0; g < ng; ++g) {
-        ptx::cp_async_wait<kStatsGroups - 1>();  // group g has landed
-        const uint4* slot = ring + (int)(g % kStatsGroups) * 8 * 256;
+    for (int64_t k = 0; k < nbox; ++k, ++it) {
+      const uint32_t b = it % kStatsBufs;
+      if (threadIdx.x == 0) s_ok = ptx::mbar_wait(&s_full[b], (it / kStatsBufs) & 1u, kWaitLimit) ? 1 : 0;
+      __syncthreads();
+      if (!s_ok) {
+        if (threadIdx.x == 0) atomicExch(p.err, kErrQuantLoad);
+        return;  // every thread leaves together; the error word reports the timeout
+      }
+      const int64_t row0 = rb0 + k * kStatsBoxRows + rl;  // this thread's first row of the box
+      const int64_t left = row0 < rb1 ? (rb1 - row0 + 31) / 32 : 0;  // this thread's rows left in the block
+      const int nv = left < 8 ? (int)left : 8;
+      if (nv > 0) {
+        const uint8_t* box = ring + b * kStatsBox;
         uint4 v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = slot[256 * j];
-        if (8 * g + 8 <= nrow)
+        for (int j = 0; j < 8; ++j) {
+          const int r = rl + 32 * j;
+          v[j] = *reinterpret_cast<const uint4*>(box + r * 128 + ((g8 ^ (r & 7)) << 4));
+        }
+#pragma unroll
+        for (int j = 1; j < 8; ++j)
+          if (j >= nv) v[j] = v[0];  // a counted row: harmless for max / min; group() drops it from the sum
+        if (nv == 8)
           group(v, 8);
         else
-          group(v, (int)(nrow - 8 * g));
-        if (g + kStatsGroups < ng) issue(g + kStatsGroups);
-        else ptx::cp_async_commit();
+          group(v, nv);
       }
-      ptx::cp_async_wait<0>();
+      __syncthreads();  // the buffer is free
+      if (threadIdx.x == 0 && k + kStatsBufs < nbox) {
+        ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
+        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64, (int32_t)(rb0 + (k + kStatsBufs) * kStatsBoxRows),
+                         &s_full[b]);
+      }
     }
     // combine the 4 row lanes of this warp that share the columns (lanes differ by 8, 16)
 #pragma unroll
