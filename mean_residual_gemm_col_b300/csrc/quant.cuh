@@ -414,14 +414,15 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
     F2 acc{0.f, 0.f};
     float m1 = -FLT_MAX, m2 = FLT_MAX;
     if (col < p.C) {
-      for (int rb = part; rb < nrb; rb += 16) {
-        float4 q[4];
+      // row blocks part, part + 4, ... in order; up to 32 row blocks in one round of loads
+      for (int rb = part; rb < nrb; rb += 32) {
+        float4 q[8];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
+        for (int j = 0; j < 8; ++j)
           q[j] = rb + 4 * j < nrb ? __ldcg(reinterpret_cast<const float4*>(p.part + (int64_t)(rb + 4 * j) * p.C + col))
                                   : make_float4(0.f, 0.f, -FLT_MAX, FLT_MAX);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
           acc = df_add(acc, F2{q[j].x, q[j].y});
           m1 = fmaxf(m1, q[j].z);
           m2 = fminf(m2, q[j].w);
