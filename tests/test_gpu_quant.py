@@ -106,3 +106,22 @@ def test_quantize_is_deterministic(cuda_lib):
     b = capi.averis_quantize(x, capi.AVERIS_MEAN_SPLIT)
     assert (a["mu"] == b["mu"]).all()
     assert (a["row"].codes == b["row"].codes).all() and (a["col"].scales == b["col"].scales).all()
+
+
+def test_split_quantize_wider_than_one_strip_per_cta(cuda_lib):
+    """More 64-column strips (1040) than strip groups of the stats pass (1024):
+    some CTAs take two strips in turn, and the quantize pass runs 520 column
+    tiles; every code and scale still bit-exact."""
+    from mean_residual_gemm_col_b300 import capi
+
+    R, C = 64, 66560
+    x = workloads.activation(workloads.rng(R * 7 + C), R, C, spike=50.0)
+    out = capi.averis_quantize(to_dev_bf16(x), capi.AVERIS_MEAN_SPLIT)
+    mu_gpu = out["mu"].cpu().numpy().astype(np.float64)
+    x64 = x.astype(np.float64)
+    ok, worst = mu_close(mu_gpu, x64, oav.column_mean(x64))
+    assert ok, f"mu off by {worst:.3g} (relative)"
+    r = oav.residual_fp32(x64, mu_gpu)
+    _check_nvfp4(out["row"], onv.quantize(r), "row layout")
+    _check_nvfp4(out["col"], onv.quantize(r.T), "column layout")
+    _check_nvfp4(out["mu_q"], onv.quantize(mu_gpu[None, :]), "mean")
