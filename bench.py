@@ -45,8 +45,8 @@ CPU_SAMPLE_TOKENS = 256
 
 
 # DRAM bytes (read + write) per GEMM launch of this step, averaged over the 12
-# GEMM launches of one ncu capture (profiles/dram_traffic_qwen3_step.md), valid
-# only for the GEMM source it was taken on.
+# GEMM launches of one ncu capture, keyed by a hash of the GEMM source the
+# capture was taken on; any other source reports null.
 GEMM_TRAFFIC = {"c8581fbd97ab5c73": 250.9e6 / 12}
 
 
@@ -110,12 +110,56 @@ def max_over_ranks(v, ws):
 
 # ----------------------------------------------------------------- clocks --
 
+class _Nvml:
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the driver)."""
+
+    REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+               "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
+
+    def __init__(self, cuda_index):
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit_v2 failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        bus = self._pci_bus_id(cuda_index)
+        if bus is None or lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) != 0:
+            n = ctypes.c_uint()
+            lib.nvmlDeviceGetCount_v2(ctypes.byref(n))
+            if lib.nvmlDeviceGetHandleByIndex_v2(0 if n.value == 1 else cuda_index, ctypes.byref(self.h)) != 0:
+                raise OSError("no NVML handle for the device")
+        self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+
+    @staticmethod
+    def _pci_bus_id(i):
+        try:
+            import torch
+
+            p = torch.cuda.get_device_properties(i)
+            return f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0"
+        except Exception:
+            return None
+
+    def sample(self):
+        u, mx, pw, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(u)) != 0:       # NVML_CLOCK_SM
+            raise OSError("nvmlDeviceGetClockInfo failed")
+        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
+        self._reasons(self.h, ctypes.byref(r))
+        return (float(u.value), float(mx.value), pw.value / 1000.0,
+                {k for k, b in self.REASONS.items() if r.value & b})
+
+
 class ClockSampler:
     """SM clock, power and throttle reasons sampled while the timed region runs.
 
-    NVML read-only queries every 10 ms on a thread (so a sub-second timed
-    region still gets tens of samples); nvidia-smi at 200 ms if NVML is not
-    available.  Only samples taken between __enter__ and __exit__ count.
+    Read-only NVML queries every 2 ms on a thread, so that even a timed region
+    of a few milliseconds gets samples; nvidia-smi at 200 ms if NVML cannot be
+    loaded.  ``mark()`` opens and closes the timed region: the summary reports
+    the samples taken inside it, and separately every sample from the start of
+    the sampler (warm-up and timed region) as the under-load record.
     """
 
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -125,43 +169,33 @@ class ClockSampler:
 
     def __init__(self, device_index):
         self.dev = device_index
-        self.rows = []       # (sm_mhz, max_mhz, power_w, set of active reason names)
+        self.rows = []       # (t, sm_mhz, max_mhz, power_w, set of active reason names)
+        self.window = [None, None]
         self.proc = None
         self.path = None
         self.thread = None
         self.stop = None
         self.nvml_error = None
 
-    def _nvml_handle(self):
-        import pynvml
+    def mark(self, which):
+        self.window[0 if which == "start" else 1] = time.perf_counter()
 
-        pynvml.nvmlInit()
-        n = pynvml.nvmlDeviceGetCount()
-        return pynvml, pynvml.nvmlDeviceGetHandleByIndex(0 if n == 1 else self.dev)
-
-    def _poll(self, nv, h):
-        bits = {"hw_slowdown": nv.nvmlClocksEventReasonHwSlowdown,
-                "hw_thermal_slowdown": nv.nvmlClocksEventReasonHwThermalSlowdown,
-                "sw_thermal_slowdown": nv.nvmlClocksEventReasonSwThermalSlowdown,
-                "sw_power_cap": nv.nvmlClocksEventReasonSwPowerCap}
+    def _poll(self, nv):
         while not self.stop.is_set():
             try:
-                r = nv.nvmlDeviceGetCurrentClocksEventReasons(h)
-                self.rows.append((float(nv.nvmlDeviceGetClockInfo(h, nv.NVML_CLOCK_SM)),
-                                  float(nv.nvmlDeviceGetMaxClockInfo(h, nv.NVML_CLOCK_SM)),
-                                  nv.nvmlDeviceGetPowerUsage(h) / 1000.0,
-                                  {k for k, b in bits.items() if r & b}))
-            except Exception:
+                self.rows.append((time.perf_counter(),) + nv.sample())
+            except Exception as e:
+                self.nvml_error = f"{type(e).__name__}: {e}"[:120]
                 break
-            time.sleep(0.01)
+            time.sleep(0.002)
 
     def __enter__(self):
         import threading
 
         try:
-            nv, h = self._nvml_handle()
+            nv = _Nvml(self.dev)
             self.stop = threading.Event()
-            self.thread = threading.Thread(target=self._poll, args=(nv, h), daemon=True)
+            self.thread = threading.Thread(target=self._poll, args=(nv,), daemon=True)
             self.thread.start()
             return self
         except Exception as e:  # no NVML: fall back to nvidia-smi
@@ -197,24 +231,36 @@ class ClockSampler:
                     return float(v)
                 except ValueError:
                     return None
+            now = time.perf_counter()
             with open(self.path) as f:
                 for ln in f:
                     p = [v.strip() for v in ln.split(",")]
                     if len(p) >= 9 and num(p[1]) is not None:
-                        self.rows.append((num(p[1]), num(p[2]), num(p[3]),
+                        self.rows.append((now, num(p[1]), num(p[2]), num(p[3]),
                                           {self.NAMES[i] for i in range(4) if p[5 + i].lower().startswith("active")}))
             os.unlink(self.path)
 
-    def summary(self):
-        if not self.rows:
+    @staticmethod
+    def _stats(rows):
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
-        sm = [r[0] for r in self.rows]
-        mx = [r[1] for r in self.rows if r[1] is not None]
-        pw = [r[2] for r in self.rows if r[2] is not None]
-        reasons = sorted(set().union(*(r[3] for r in self.rows)))
-        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
-               "power_w_max": max(pw) if pw else None, "reasons": reasons, "samples": len(self.rows),
-               "source": "nvml 10 ms" if self.thread is not None else "nvidia-smi 200 ms"}
+        sm = [r[1] for r in rows]
+        mx = [r[2] for r in rows if r[2] is not None]
+        pw = [r[3] for r in rows if r[3] is not None]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": sorted(set().union(*(r[4] for r in rows))), "samples": len(rows)}
+
+    def summary(self):
+        t0, t1 = self.window
+        inside = [r for r in self.rows if t0 is not None and t1 is not None and t0 <= r[0] <= t1]
+        if self.thread is None:            # nvidia-smi rows carry no time of their own
+            inside = list(self.rows)
+        out = self._stats(inside)
+        out["source"] = "nvml 2 ms" if self.thread is not None else "nvidia-smi 200 ms"
+        out["window"] = "timed region"
+        out["under_load"] = self._stats(self.rows)
+        out["under_load"]["window"] = "warm-up and timed region"
         if self.nvml_error:
             out["nvml_error"] = self.nvml_error
         return out
@@ -403,18 +449,19 @@ def run_ours(args, rank, ws):
     ggraphs = {k: capture(v) for k, v in groups.items()}
     stream = torch.cuda.current_stream()
 
-    for _ in range(args.warmup):
-        graphs["averis"].replay()
-    torch.cuda.synchronize()
-
     # ---- headline: K steps of the Averis fwd+bwd, barrier + sync on both sides
     with ClockSampler(torch.cuda.current_device()) as clk:
+        for _ in range(args.warmup):
+            graphs["averis"].replay()
+        torch.cuda.synchronize()
         barrier(ws)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
+        clk.mark("start")
         torch.cuda.nvtx.range_push("averis_timed")
         ms = time_graph(graphs["averis"], args.steps, stream)
         torch.cuda.nvtx.range_pop()
+        clk.mark("end")
         wall = time.perf_counter() - t0
         barrier(ws)
     clocks = clk.summary()
@@ -778,6 +825,20 @@ def stack_comparison(steps=3, warmup=2):
 
 # --------------------------------------------------------- CPU baseline ----
 
+def blas_threads():
+    """Threads of the BLAS NumPy calls into (threadpoolctl), else the OpenMP setting."""
+    try:
+        from threadpoolctl import threadpool_info
+
+        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    v = os.environ.get("OMP_NUM_THREADS")
+    return int(v) if v and v.isdigit() else None
+
+
 def cpu_baseline(target_s=10.0):
     """The oracle, as it stands, on a bounded sample of the workload.
 
@@ -787,7 +848,7 @@ def cpu_baseline(target_s=10.0):
     """
     from oracle import averis as oav
 
-    threads = os.environ.get("OMP_NUM_THREADS") or str(os.cpu_count())
+    threads = blas_threads()
     tok = CPU_SAMPLE_TOKENS
     total_flops = 0.0
     t_total = 0.0
@@ -803,8 +864,9 @@ def cpu_baseline(target_s=10.0):
         rep += 1
         if t_total >= target_s:
             break
-    return {"value": round(total_flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
-            "threads": threads, "kind": "oracle",
+    return {"value": round(total_flops / t_total / 1e12, 6), "unit": "TFLOP/s",
+            "cores": threads or os.cpu_count(), "host_cpus": os.cpu_count(), "blas_threads": threads,
+            "kind": "oracle",
             "sample": f"{rep} x ({tok} of {L} tokens of each of the 4 linears, fwd+bwd), float64 NumPy, "
                       f"{t_total:.1f} s"}
 

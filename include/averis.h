@@ -26,8 +26,13 @@
  *
  * Conventions for every call:
  *  - Pointers marked "device" are device memory of the current CUDA device,
- *    allocated and owned by the caller; the library allocates nothing and
- *    keeps no state besides per-device kernel attributes.
+ *    allocated and owned by the caller.  The library makes no allocation.
+ *    Every context that loads it holds two file-scope device objects: a
+ *    4-byte error word and the AVERIS_NOALLOC_SCRATCH_BYTES scratch array of
+ *    averis_quantize_noalloc.  Per device, the library caches the SM count,
+ *    those objects' device addresses and the kernel attributes it set.  These
+ *    caches are keyed by device ordinal and are not rebuilt, so do not keep
+ *    using the library on a device after cudaDeviceReset.
  *  - All work is enqueued on `stream`; a call returns as soon as it is
  *    enqueued.  The status reports argument errors (nothing is enqueued then)
  *    and launch errors.  Device-side wait timeouts are reported through
@@ -36,9 +41,12 @@
  *    be 16-byte aligned (256-byte for workspaces).
  *  - Workspaces: the first AVERIS_WORKSPACE_CTRL_BYTES bytes of every
  *    workspace are a control block (tickets and running maxima) that must be
- *    zero before the workspace is first used; every call leaves it zero
- *    again, so zero-fill a workspace once when allocating it.  The rest is
- *    scratch.
+ *    zero before the workspace is first used.  Every call that runs to
+ *    completion leaves it zero again, including a call whose device-side
+ *    waits gave up (AVERIS_ERR_TIMEOUT).  So zero-fill a workspace once when
+ *    allocating it.  Zero it again only after a call that returned
+ *    AVERIS_ERR_CUDA, since then some of its kernels may not have run.  The
+ *    rest of the workspace is scratch.
  *  - Calls that share a workspace or an output must not overlap in time.
  *  - Sizes: cols of every NVFP4 tensor and the m, n of a linear layer must be
  *    multiples of 16; the token count l may be any value >= 1 (a partial last
@@ -287,10 +295,30 @@ const char* averis_status_string(averis_status status);
 
 /*
  * Reads and clears the device error word that kernels set when a bounded
- * wait gives up.  Synchronizes `stream`.  Returns AVERIS_OK or AVERIS_ERR_TIMEOUT;
- * *where (if not NULL) receives the code of the wait that gave up.
+ * wait gives up (about one second of SM clock).  Synchronizes `stream`.
+ * Returns AVERIS_OK or AVERIS_ERR_TIMEOUT; *where (if not NULL) receives the
+ * code of the wait that gave up:
+ *   1 GEMM TMA producer, 2 GEMM MMA issuer, 3 GEMM epilogue, 4 GEMM drain,
+ *   5 quantize pass (an input box or tile never arrived), 6 GEMM scale feed.
+ * The results of the calls that timed out are invalid.  When it reports a
+ * timeout it also zeroes the control block of averis_quantize_noalloc's
+ * scratch, whose callers cannot reach it.
  */
 averis_status averis_last_device_error(cudaStream_t stream, int* where);
+
+/*
+ * averis_debug_starve_next_quantize -- diagnostics of the timeout path.  The
+ * method has no counterpart of this call.  The next averis_quantize,
+ * averis_quantize_weight or averis_quantize_noalloc call, or the next quantize
+ * step of a linear call, from any host thread, runs its statistics pass without
+ * requesting its input.  Every bounded wait of that pass for its input then
+ * gives up after `wait_cycles` SM clock cycles.  That call's results are
+ * invalid, and averis_last_device_error then reports AVERIS_ERR_TIMEOUT with
+ * code 5.  The workspace's control block is left zero for the next call.  Only
+ * a host-side switch: no copy is left in flight and nothing faults on the GPU.
+ * wait_cycles must lie in [1e4, 2^31]; otherwise AVERIS_ERR_INVALID_ARG.
+ */
+averis_status averis_debug_starve_next_quantize(long long wait_cycles);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int averis_version(void);

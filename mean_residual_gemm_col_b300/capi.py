@@ -35,7 +35,7 @@ EXPORTS = (
     "averis_linear_fwd", "averis_linear_bwd", "nvfp4_linear_fwd", "nvfp4_linear_bwd",
     "averis_status_string", "averis_last_device_error", "averis_version", "averis_quantize_noalloc",
     "averis_grouped_linear_fwd_workspace_bytes", "averis_grouped_linear_bwd_workspace_bytes",
-    "averis_grouped_linear_fwd", "averis_grouped_linear_bwd",
+    "averis_grouped_linear_fwd", "averis_grouped_linear_bwd", "averis_debug_starve_next_quantize",
 )
 
 
@@ -84,6 +84,7 @@ def _declare(lib):
         "averis_grouped_linear_bwd_workspace_bytes": (SZ, [P, I64, I64, I64, U]),
         "averis_grouped_linear_fwd": (I, [P, P, I64, I64, I64, P, U, P, P, P, SZ, P]),
         "averis_grouped_linear_bwd": (I, [P, P, I64, I64, I64, P, P, U, P, P, P, SZ, P]),
+        "averis_debug_starve_next_quantize": (I, [ctypes.c_longlong]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -430,6 +431,11 @@ def averis_last_device_error(device=None) -> int:
     if st not in (0, 5):
         _check(st, "averis_last_device_error")
     return where.value
+
+
+def debug_starve_next_quantize(wait_cycles: int) -> None:
+    """Make the next quantize call's waits for its input run out (timeout-path diagnostics)."""
+    _check(load().averis_debug_starve_next_quantize(int(wait_cycles)), "averis_debug_starve_next_quantize")
 
 
 def status_string(code: int) -> str:

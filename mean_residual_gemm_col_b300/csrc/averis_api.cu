@@ -32,6 +32,11 @@ struct DeviceInfo {
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mutex;
 
+// Diagnostics of the timeout path (averis_debug_starve_next_quantize): when
+// non-zero, the next quantize call's statistics pass requests no input and
+// waits at most this many SM cycles for it.
+long long g_starve_next = 0;
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -220,6 +225,15 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   sp.hadamard = had ? 1 : 0;
   sp.mu = mu;
   sp.err = dev->err_word;
+  sp.wait_limit = kWaitLimit;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_starve_next > 0) {
+      sp.starve = 1;
+      sp.wait_limit = g_starve_next;
+      g_starve_next = 0;
+    }
+  }
   CUtensorMap tstats;  // X in boxes of 64 columns x 256 rows for the stats pass
   if (!encode_2d(&tstats, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x), (uint64_t)C, (uint64_t)R,
                  (uint64_t)C * 2, 64u, (uint32_t)kStatsBoxRows))
@@ -242,6 +256,7 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   }
   qp.ctrl = ctrl;
   qp.err = dev->err_word;
+  qp.wait_limit = kWaitLimit;
   qp.hadamard = had ? 1 : 0;
   if (out_row != nullptr) {
     qp.row_codes = out_row->codes;
@@ -460,6 +475,10 @@ averis_status linear_bwd_impl(const void* d, int64_t l, int64_t m, int64_t n, co
                    n, flags & ~AVERIS_OUT_BF16, s, /*early_start=*/true);
 }
 
+// Zeroes the control block of the allocation-free call's scratch on this
+// device (if that call was ever made here), ordered after `stream`.
+averis_status noalloc_reset_ctrl(cudaStream_t stream);
+
 }  // namespace
 
 // ================================================================ C ABI ==
@@ -638,9 +657,20 @@ averis_status averis_last_device_error(cudaStream_t stream, int* where) {
   if (v != 0) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return AVERIS_ERR_CUDA;
+    // the kernels leave a control block zero even when a wait gives up; the
+    // library-owned one of the allocation-free call is cleared here as well,
+    // since its callers have no way to do it themselves
+    if (noalloc_reset_ctrl(stream) != AVERIS_OK) return AVERIS_ERR_CUDA;
   }
   if (where != nullptr) *where = v;
   return v == 0 ? AVERIS_OK : AVERIS_ERR_TIMEOUT;
+}
+
+averis_status averis_debug_starve_next_quantize(long long wait_cycles) {
+  if (wait_cycles < 10000 || wait_cycles > kWaitLimit) return AVERIS_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  g_starve_next = wait_cycles;
+  return AVERIS_OK;
 }
 
 int averis_version(void) { return 100; }
@@ -671,6 +701,19 @@ averis_status noalloc_scratch(void** out) {
   }
   *out = g_noalloc_addr[dev];
   return AVERIS_OK;
+}
+
+averis_status noalloc_reset_ctrl(cudaStream_t stream) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return AVERIS_ERR_CUDA;
+  void* addr = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    addr = g_noalloc_addr[dev];
+  }
+  if (addr == nullptr) return AVERIS_OK;
+  if (cudaMemsetAsync(addr, 0, AVERIS_WORKSPACE_CTRL_BYTES, stream) != cudaSuccess) return AVERIS_ERR_CUDA;
+  return cudaStreamSynchronize(stream) == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA;
 }
 
 }  // namespace

@@ -228,6 +228,10 @@ struct StatsParams {
   int split;          // mean split on
   int hadamard;       // rotation on (the rotated residual's maximum comes from the amax pass)
   float* mu;          // [C] out (split)
+  long long wait_limit;  // bound of every wait, in SM clock cycles
+  // diagnostics only: issue no input loads, so that every wait for a box runs
+  // out (exercises the timeout path with no copy in flight)
+  int starve;
 };
 
 // Column statistics in one pass over X, with the combine fused in.
@@ -272,7 +276,8 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
   const int64_t rb0 = (int64_t)blockIdx.y * p.rows_per;
   const int64_t rb1 = min(p.R, rb0 + p.rows_per);
 
-  for (int strip = blockIdx.x; strip < p.nstrips; strip += gridDim.x) {
+  bool failed = false;  // a box never arrived (uniform over the CTA)
+  for (int strip = blockIdx.x; strip < p.nstrips && !failed; strip += gridDim.x) {
     // column pairs (2w, 2w+1): Kahan-compensated binary32 sums, packed bf16 max / min
     uint64_t s2[4], c2[4];
     uint32_t mx2[4], mn2[4];
@@ -313,7 +318,7 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
     // rl, rl + 32, ... of a box are one 8-row group.  Rows past this CTA's block
     // are left out (max / min see a repeat of a counted row, the sum zeros).
     const int64_t nbox = (rb1 - rb0 + kStatsBoxRows - 1) / kStatsBoxRows;
-    if (threadIdx.x == 0)
+    if (threadIdx.x == 0 && !p.starve)
       for (int64_t k = 0; k < kStatsBufs && k < nbox; ++k) {
         const uint32_t b = (it + (uint32_t)k) % kStatsBufs;
         ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
@@ -321,11 +326,21 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
       }
     for (int64_t k = 0; k < nbox; ++k, ++it) {
       const uint32_t b = it % kStatsBufs;
-      if (threadIdx.x == 0) s_ok = ptx::mbar_wait(&s_full[b], (it / kStatsBufs) & 1u, kWaitLimit) ? 1 : 0;
+      if (threadIdx.x == 0) s_ok = ptx::mbar_wait(&s_full[b], (it / kStatsBufs) & 1u, p.wait_limit) ? 1 : 0;
       __syncthreads();
       if (!s_ok) {
-        if (threadIdx.x == 0) atomicExch(p.err, kErrQuantLoad);
-        return;  // every thread leaves together; the error word reports the timeout
+        // every thread gives up together: report, let the boxes still in flight
+        // land (bounded), and still take the ticket below so that the control
+        // block returns to zero; the results of this call are invalid
+        if (threadIdx.x == 0) {
+          atomicExch(p.err, kErrQuantLoad);
+          const int64_t issued = p.starve ? k : min(nbox, k + (int64_t)kStatsBufs);
+          for (int64_t j = k + 1; j < issued; ++j)
+            ptx::mbar_wait(&s_full[(it + (uint32_t)(j - k)) % kStatsBufs],
+                           ((it + (uint32_t)(j - k)) / kStatsBufs) & 1u, p.wait_limit);
+        }
+        failed = true;
+        break;
       }
       const int64_t row0 = rb0 + k * kStatsBoxRows + rl;  // this thread's first row of the box
       const int64_t left = row0 < rb1 ? (rb1 - row0 + 31) / 32 : 0;  // this thread's rows left in the block
@@ -353,6 +368,7 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
                          &s_full[b]);
       }
     }
+    if (failed) break;
     // combine the 4 row lanes of this warp that share the columns (lanes differ by 8, 16)
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -628,6 +644,7 @@ struct QuantParams {
   // CTAs [0, mean_ctas) quantize the mean and compute the rank-one row; the
   // rest quantize tiles
   int mean_ctas;
+  long long wait_limit;  // bound of every wait, in SM clock cycles
   // optional rank-one row (split only): r[N] = deq(mu_q) deq(W)^T, with W an
   // NVFP4 [N, C] tensor blocked along C (the blocking of the mean)
   const uint8_t* w_codes;
@@ -896,12 +913,14 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
   }
 
   int i = 0;
+  bool failed = false;
   for (int tile = mean_cta ? ntiles : tcta; tile < ntiles; tile += ntcta, ++i) {
     const int b = i % kQBufs;
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     const int64_t r0 = (int64_t)tr * kQTile, c0 = (int64_t)tc * kQTile;
-    if (!ptx::mbar_wait(&full[b], (uint32_t)((i / kQBufs) & 1), kWaitLimit)) {
+    if (!ptx::mbar_wait(&full[b], (uint32_t)((i / kQBufs) & 1), p.wait_limit)) {
       if (lane == 0) atomicExch(p.err, kErrQuantLoad);
+      failed = true;
       break;
     }
     const uint8_t* buf = sm + b * kQTileBytes;
@@ -949,6 +968,12 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
         issue_mu(tile + kQBufs * ntcta, b);
       }
     }
+  }
+  if (failed && tid == 0) {
+    // this call's results are invalid; let the tiles already requested for this
+    // CTA's buffers land (bounded) before its shared memory is given up
+    for (int j = i; j < i + kQBufs; ++j)
+      if (tcta + j * ntcta < ntiles) ptx::mbar_wait(&full[j % kQBufs], (uint32_t)((j / kQBufs) & 1), p.wait_limit);
   }
   if (AMAX_ONLY) {
     // rotated maxima, read by the quantize pass that follows

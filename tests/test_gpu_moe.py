@@ -53,3 +53,53 @@ def test_grouped_linear_matches_per_expert_oracle(cuda_lib, split):
         assert rel_fro(y[a:b], f.y) < TOL, e
         assert rel_fro(dx[a:b], bw.dx) < TOL, e
         assert rel_fro(dw[e].cpu().numpy(), bw.dw) < TOL, e
+
+
+@pytest.mark.parametrize("linear", ["gate_up", "down"])
+def test_grouped_moe_expert_ffn_full_shape(cuda_lib, linear):
+    """The mixture-of-experts expert FFN at its benchmarked shape: hidden 2048, 64
+    experts, top-8 of 16384 tokens with Zipf(1.1) popularity, expert FFN 768.  The
+    smallest, the median-size and the largest expert are compared with the
+    single-layer oracle over their own rows (means per expert, given the GPU's),
+    Averis and vanilla; the mean of each is checked against the exact mean."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+    from tests.gpu_util import mu_close
+
+    cfg = workloads.MOE
+    counts = workloads.moe_routing(0, cfg["tokens"], cfg["experts"], cfg["top_k"], cfg["zipf"])
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    L = int(offsets[-1])
+    m, n = (cfg["hidden"], 2 * cfg["ffn"]) if linear == "gate_up" else (cfg["ffn"], cfg["hidden"])
+    x = workloads.torch_activation(31, L, m, spike=workloads.QWEN3_SPIKE, device="cuda")
+    _, _, d = workloads.torch_linear_case(41, L, 16, n, device="cuda")
+    order = np.argsort(counts, kind="stable")
+    picks = sorted({int(order[0]), int(order[len(order) // 2]), int(order[-1])})
+    ws = {e: workloads.torch_linear_case(100 + e, 16, m, n, device="cuda")[1] for e in range(cfg["experts"])}
+    w_n, w_m = zip(*[capi.averis_quantize_weight(ws[e]) for e in range(cfg["experts"])])
+    X, D = x.float().cpu().numpy(), d.float().cpu().numpy()
+    for split in (True, False):
+        gl = capi.GroupedLinear(offsets, m, n, list(w_m), list(w_n), "cuda")
+        flags = capi.AVERIS_MEAN_SPLIT if split else 0
+        y = gl.fwd(x, flags).cpu().numpy()
+        dx, dw = gl.bwd(d, flags)
+        dx = dx.cpu().numpy()
+        torch.cuda.synchronize()
+        assert capi.averis_last_device_error() == 0
+        for e in picks:
+            a, b = int(offsets[e]), int(offsets[e + 1])
+            xe, de = X[a:b].astype(np.float64), D[a:b].astype(np.float64)
+            mu_x = mu_d = None
+            if split:
+                mu_x = gl.states[e].mu.cpu().numpy().astype(np.float64)
+                mu_d = capi.averis_quantize(d[a:b].contiguous(), capi.AVERIS_MEAN_SPLIT, want_row=False,
+                                            want_col=False)["mu"].cpu().numpy().astype(np.float64)
+                assert mu_close(mu_x, xe, oav.column_mean(xe))[0], e
+                assert mu_close(mu_d, de, oav.column_mean(de))[0], e
+            we = ws[e].float().cpu().numpy().astype(np.float64)
+            f, bw = oav.linear_fwd_bwd(xe, we, de, do_split=split, mu_x=mu_x, mu_d=mu_d)
+            tag = f"{linear} expert {e} ({b - a} rows) split={split}"
+            assert rel_fro(y[a:b], f.y) < TOL, tag
+            assert rel_fro(dx[a:b], bw.dx) < TOL, tag
+            assert rel_fro(dw[e].cpu().numpy(), bw.dw) < TOL, tag
+        del gl
