@@ -130,6 +130,9 @@ class _Nvml:
                 raise OSError("no NVML handle for the device")
         self._reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
             lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        mx = ctypes.c_uint()
+        lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.max_mhz = float(mx.value)
 
     @staticmethod
     def _pci_bus_id(i):
@@ -141,21 +144,23 @@ class _Nvml:
         except Exception:
             return None
 
-    def sample(self):
-        u, mx, pw, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+    def sample(self, with_power=True):
+        u, r = ctypes.c_uint(), ctypes.c_ulonglong()
         if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(u)) != 0:       # NVML_CLOCK_SM
             raise OSError("nvmlDeviceGetClockInfo failed")
-        self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
-        self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(pw))
         self._reasons(self.h, ctypes.byref(r))
-        return (float(u.value), float(mx.value), pw.value / 1000.0,
-                {k for k, b in self.REASONS.items() if r.value & b})
+        pw = None
+        if with_power:                      # the slowest query: not on every tick
+            p = ctypes.c_uint()
+            if self.lib.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(p)) == 0:
+                pw = p.value / 1000.0
+        return (float(u.value), self.max_mhz, pw, {k for k, b in self.REASONS.items() if r.value & b})
 
 
 class ClockSampler:
     """SM clock, power and throttle reasons sampled while the timed region runs.
 
-    Read-only NVML queries every 2 ms on a thread, so that even a timed region
+    Read-only NVML queries every millisecond or so on a thread, so that even a timed region
     of a few milliseconds gets samples; nvidia-smi at 200 ms if NVML cannot be
     loaded.  ``mark()`` opens and closes the timed region: the summary reports
     the samples taken inside it, and separately every sample from the start of
@@ -181,13 +186,16 @@ class ClockSampler:
         self.window[0 if which == "start" else 1] = time.perf_counter()
 
     def _poll(self, nv):
+        k = 0
         while not self.stop.is_set():
             try:
-                self.rows.append((time.perf_counter(),) + nv.sample())
+                t = time.perf_counter()
+                self.rows.append((t,) + nv.sample(with_power=k % 10 == 0))
             except Exception as e:
                 self.nvml_error = f"{type(e).__name__}: {e}"[:120]
                 break
-            time.sleep(0.002)
+            k += 1
+            time.sleep(0.001)
 
     def __enter__(self):
         import threading
@@ -257,7 +265,7 @@ class ClockSampler:
         if self.thread is None:            # nvidia-smi rows carry no time of their own
             inside = list(self.rows)
         out = self._stats(inside)
-        out["source"] = "nvml 2 ms" if self.thread is not None else "nvidia-smi 200 ms"
+        out["source"] = "nvml ~1 ms" if self.thread is not None else "nvidia-smi 200 ms"
         out["window"] = "timed region"
         out["under_load"] = self._stats(self.rows)
         out["under_load"]["window"] = "warm-up and timed region"
@@ -848,7 +856,6 @@ def cpu_baseline(target_s=10.0):
     """
     from oracle import averis as oav
 
-    threads = blas_threads()
     tok = CPU_SAMPLE_TOKENS
     total_flops = 0.0
     t_total = 0.0
@@ -864,6 +871,7 @@ def cpu_baseline(target_s=10.0):
         rep += 1
         if t_total >= target_s:
             break
+    threads = blas_threads()                # after the oracle ran: its BLAS is loaded by now
     return {"value": round(total_flops / t_total / 1e12, 6), "unit": "TFLOP/s",
             "cores": threads or os.cpu_count(), "host_cpus": os.cpu_count(), "blas_threads": threads,
             "kind": "oracle",

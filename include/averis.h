@@ -41,12 +41,13 @@
  *    be 16-byte aligned (256-byte for workspaces).
  *  - Workspaces: the first AVERIS_WORKSPACE_CTRL_BYTES bytes of every
  *    workspace are a control block (tickets and running maxima) that must be
- *    zero before the workspace is first used.  Every call that runs to
- *    completion leaves it zero again, including a call whose device-side
- *    waits gave up (AVERIS_ERR_TIMEOUT).  So zero-fill a workspace once when
- *    allocating it.  Zero it again only after a call that returned
- *    AVERIS_ERR_CUDA, since then some of its kernels may not have run.  The
- *    rest of the workspace is scratch.
+ *    zero before the workspace is first used; its place does not depend on
+ *    the sizes of a call, so one workspace serves calls of any shape.  Every
+ *    call that runs to completion leaves it zero again, including a call
+ *    whose device-side waits gave up (AVERIS_ERR_TIMEOUT).  So zero-fill the
+ *    control block once when allocating a workspace, and again only after a
+ *    call that returned AVERIS_ERR_CUDA, since then some of its kernels may
+ *    not have run.  The rest of a workspace is scratch.
  *  - Calls that share a workspace or an output must not overlap in time.
  *  - Sizes: cols of every NVFP4 tensor and the m, n of a linear layer must be
  *    multiples of 16; the token count l may be any value >= 1 (a partial last
@@ -73,7 +74,7 @@ typedef enum {
 } averis_status;
 
 /* Size of the control block at the head of every workspace (zero at rest). */
-#define AVERIS_WORKSPACE_CTRL_BYTES 4352
+#define AVERIS_WORKSPACE_CTRL_BYTES 12544
 
 /* flags */
 #define AVERIS_MEAN_SPLIT 1u  /* subtract the column mean (Averis); clear = vanilla NVFP4 */

@@ -5,6 +5,7 @@
 #include <cstring>
 #include <algorithm>
 #include <mutex>
+#include <vector>
 
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -18,6 +19,10 @@ namespace {
 using namespace averis;
 
 constexpr int kMaxDevices = 64;
+#ifndef AVERIS_GEMM_SFB_FULL
+#define AVERIS_GEMM_SFB_FULL 1
+#endif
+constexpr bool kSfbFull = AVERIS_GEMM_SFB_FULL != 0;
 constexpr int kStatsTargetCtas = 296;  // CTA count target of the stats pass (one wave at 2 per SM of a B300)
 
 __device__ int g_device_error = 0;
@@ -28,6 +33,7 @@ struct DeviceInfo {
   int cc_major = 0, cc_minor = 0;
   int* err_word = nullptr;
   bool attrs_set = false;
+  int gemm_pairs = 0;  // clusters of two GEMM CTAs resident at once (the persistent grid's size)
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mutex;
@@ -79,6 +85,16 @@ averis_status device_info(DeviceInfo** out) {
   if (!d.attrs_set) {
     averis_status st = set_attrs();
     if (st != AVERIS_OK) return st;
+    // a persistent grid larger than the clusters that can be resident together
+    // would leave its last pairs to run after the others: size it to that count
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (d.sms / 2));
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = GemmCfg<kSfbFull>::SMEM;
+    int pairs = 0;
+    if (cudaOccupancyMaxActiveClusters(&pairs, gemm_nvfp4_kernel<true, kSfbFull, 1>, &cfg) != cudaSuccess || pairs < 1)
+      return AVERIS_ERR_CUDA;
+    d.gemm_pairs = std::min(pairs, d.sms / 2);
     d.attrs_set = true;
   }
   *out = &d;
@@ -97,11 +113,29 @@ averis_status set_attrs() {
   if (cudaFuncSetAttribute(split_quant_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM) !=
+  if (cudaFuncSetAttribute(colstats_grouped_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatsSmem) !=
       cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg::SMEM) !=
-      cudaSuccess)
+  if (cudaFuncSetAttribute(split_quant_grouped_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kQSmem) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(split_quant_grouped_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kQSmem) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(split_quant_grouped_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kQSmem) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<false, kSfbFull, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<true, kSfbFull, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<false, kSfbFull, kMaxGemmGroups>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<true, kSfbFull, kMaxGemmGroups>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }
@@ -320,63 +354,356 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   return AVERIS_OK;
 }
 
+// ------------------------------------------------------ grouped quantize --
+
+// One row group (expert) of a grouped quantize: rows row0 .. row0+rows-1 of
+// the grouped input, its own outputs (as in quantize_impl) and optionally its
+// own rank-one row r_out = deq(mu_q) deq(r_w)^T.
+struct GroupSpec {
+  int64_t row0 = 0, rows = 0;
+  float* mu = nullptr;
+  const averis_nvfp4* mu_q = nullptr;
+  float* mu_hat = nullptr;
+  const averis_nvfp4* out_row = nullptr;
+  const averis_nvfp4* out_col = nullptr;
+  const averis_nvfp4* r_w = nullptr;
+  float* r_out = nullptr;
+};
+
+// Stats geometry shared by the groups of one grouped call: the same strip
+// groups, one row-block height, about four waves of CTAs over all rows.
+struct GroupedGeom {
+  int gx, nstrips;
+  int64_t rows_per;
+};
+GroupedGeom grouped_geom(int64_t L, int64_t C, int ngroups) {
+  GroupedGeom g;
+  g.nstrips = (int)cdiv(C, 64);
+  g.gx = std::min(g.nstrips, (int)kMaxStripGroups);
+  const int64_t target = std::max<int64_t>(ngroups, cdiv(4 * kStatsTargetCtas, g.gx));
+  g.rows_per = std::max<int64_t>(256, cdiv(cdiv(L, target), 32) * 32);
+  return g;
+}
+// Per-group control words (strip tickets and maxima, zero at rest) and row-block partials.
+size_t group_ctrl_bytes(const GroupedGeom& g) { return align256((size_t)(kCtrlStrip + g.gx) * sizeof(unsigned)); }
+size_t group_part_bytes(const GroupedGeom& g, int64_t rows, int64_t C) {
+  return align256((size_t)cdiv(rows, g.rows_per) * (size_t)C * sizeof(ColPartial));
+}
+size_t grouped_quant_ws_bytes(const int64_t* rows, int ng, int64_t C) {
+  int64_t L = 0;
+  for (int e = 0; e < ng; ++e) L += rows[e];
+  const GroupedGeom g = grouped_geom(L, C, std::min(ng, kMaxGroups));
+  size_t b = 0;
+  for (int e = 0; e < ng; ++e)
+    if (rows[e] > 0) b += group_ctrl_bytes(g) + group_part_bytes(g, rows[e], C);
+  return std::max<size_t>(b, 256);
+}
+
+// The quantize pass of up to kMaxGroups groups of one grouped input x
+// [L, C]: one stats launch and one quantize launch (two with the rotation)
+// for all of them.  Groups with no rows are skipped.  ws: the groups'
+// control words and partials, laid out in group order (zero at rest).
+averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsigned flags, const GroupSpec* gs, int ng,
+                                     const GroupedGeom& geo, uint8_t* ws, DeviceInfo* dev, cudaStream_t s) {
+  const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
+  const bool had = (flags & AVERIS_HADAMARD16) != 0;
+  GroupedStatsParams sp{};
+  GroupedQuantParams qp{};
+  GroupedQuantParams ap{};  // rotated-maximum pass: tiles only
+  int n = 0, rbs = 0, ctas = 0, actas = 0;
+  int64_t tiles_all = 0;
+  for (int e = 0; e < ng; ++e)
+    if (gs[e].rows > 0) tiles_all += cdiv(gs[e].rows, kQTile) * cdiv(C, kQTile);
+  const int64_t budget = kQCtasPerSm * (int64_t)dev->sms;  // tile CTAs of one wave, shared out by tiles
+  long long starve = 0;
+  {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    std::swap(starve, g_starve_next);
+  }
+  for (int e = 0; e < ng; ++e) {
+    const GroupSpec& G = gs[e];
+    if (G.rows <= 0) continue;
+    unsigned* ctrl = reinterpret_cast<unsigned*>(ws);
+    ws += group_ctrl_bytes(geo);
+    ColPartial* part = reinterpret_cast<ColPartial*>(ws);
+    ws += group_part_bytes(geo, G.rows, C);
+    const int nrb = (int)cdiv(G.rows, geo.rows_per);
+    StatsParams& st = sp.g[n];
+    st.x = static_cast<const __nv_bfloat16*>(x);
+    st.R = G.rows;
+    st.C = C;
+    st.rows_per = cdiv(cdiv(G.rows, nrb), 32) * 32;
+    st.nstrips = geo.nstrips;
+    st.part = part;
+    st.ctrl = ctrl;
+    st.err = dev->err_word;
+    st.split = split ? 1 : 0;
+    st.hadamard = had ? 1 : 0;
+    st.mu = G.mu;
+    st.wait_limit = starve > 0 ? starve : kWaitLimit;
+    st.starve = starve > 0 ? 1 : 0;
+    st.row_base = G.row0;
+    sp.rb0[n] = rbs;
+    rbs += (int)cdiv(G.rows, st.rows_per);
+
+    QuantParams& q = qp.g[n];
+    q.R = G.rows;
+    q.C = C;
+    q.mu = split ? G.mu : nullptr;
+    if (split) {
+      q.mu_codes = G.mu_q->codes;
+      q.mu_scales = G.mu_q->scales;
+      q.mu_ts = G.mu_q->tensor_scale;
+      q.mu_hat = G.mu_hat;
+      q.mu_kc = cdiv(C, 64);
+    }
+    q.ctrl = ctrl;
+    q.err = dev->err_word;
+    q.wait_limit = kWaitLimit;
+    q.hadamard = had ? 1 : 0;
+    if (G.out_row != nullptr) {
+      q.row_codes = G.out_row->codes;
+      q.row_scales = G.out_row->scales;
+      q.row_ts = G.out_row->tensor_scale;
+      q.row_ld = averis_nvfp4_ld(C);
+      q.row_kc = cdiv(C, 64);
+    }
+    if (G.out_col != nullptr) {
+      q.col_codes = G.out_col->codes;
+      q.col_scales = G.out_col->scales;
+      q.col_ts = G.out_col->tensor_scale;
+      q.col_ld = averis_nvfp4_ld(G.rows);
+      q.col_kc = cdiv(G.rows, 64);
+    }
+    q.tiles_r = (int)cdiv(G.rows, kQTile);
+    q.tiles_c = (int)cdiv(C, kQTile);
+    if (G.out_row == nullptr && G.out_col == nullptr) q.tiles_r = 0;
+    q.row_base = G.row0;
+    q.mean_ctas = 0;
+    if (split) {
+      q.mean_ctas = 1;
+      if (G.r_w != nullptr) {
+        q.w_codes = G.r_w->codes;
+        q.w_scales = G.r_w->scales;
+        q.w_ts = G.r_w->tensor_scale;
+        q.w_rows = G.r_w->rows;
+        q.w_ld = averis_nvfp4_ld(C);
+        q.w_kc = cdiv(C, 64);
+        q.r_out = G.r_out;
+        q.mean_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(8, cdiv(G.r_w->rows * C, (int64_t)1 << 19)));
+      }
+    }
+    const int64_t tiles = (int64_t)q.tiles_r * q.tiles_c;
+    const int tile_ctas =
+        tiles == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(tiles, budget * tiles / std::max<int64_t>(1, tiles_all)));
+    qp.cta0[n] = ctas;
+    ctas += std::max(1, q.mean_ctas + tile_ctas);
+    ap.g[n] = q;
+    ap.g[n].mean_ctas = 0;
+    ap.cta0[n] = actas;
+    actas += std::max(1, tile_ctas);
+    ++n;
+  }
+  if (n == 0) return AVERIS_OK;
+  sp.rb0[n] = rbs;
+  sp.ngroups = n;
+  qp.cta0[n] = ctas;
+  qp.ngroups = n;
+  ap.cta0[n] = actas;
+  ap.ngroups = n;
+
+  CUtensorMap tstats, tx;
+  if (!encode_2d(&tstats, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x), (uint64_t)C, (uint64_t)L,
+                 (uint64_t)C * 2, 64u, (uint32_t)kStatsBoxRows))
+    return AVERIS_ERR_CUDA;
+  if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x), (uint64_t)C, (uint64_t)L,
+                 (uint64_t)C * 2, 64u, (uint32_t)kQTile))
+    return AVERIS_ERR_CUDA;
+  if (launch_pdl(colstats_grouped_kernel, dim3(geo.gx, rbs), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (had && launch_pdl(split_quant_grouped_kernel<true, true>, dim3(actas), dim3(kQThreads), kQSmem, s, tx, ap) !=
+                 cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  auto* qk = had ? split_quant_grouped_kernel<false, true> : split_quant_grouped_kernel<false, false>;
+  if (launch_pdl(qk, dim3(ctas), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess) return AVERIS_ERR_CUDA;
+  return AVERIS_OK;
+}
+
+// All groups of a grouped input, kMaxGroups at a time.  Checks every group's
+// outputs; rows of the groups must tile [0, L) in order.
+averis_status grouped_quantize_impl(const void* x, int64_t L, int64_t C, unsigned flags, const GroupSpec* gs, int ng,
+                                    void* ws, size_t ws_bytes, cudaStream_t s) {
+  if (x == nullptr || gs == nullptr || ng < 1 || L < 1 || C < 16 || C % 16 != 0 || !aligned(x, 16))
+    return AVERIS_ERR_INVALID_ARG;
+  if (L > (int64_t)1 << 31 || C > (int64_t)1 << 31) return AVERIS_ERR_INVALID_ARG;
+  const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
+  if (split && C > kMaxSplitCols) return AVERIS_ERR_INVALID_ARG;
+  std::vector<int64_t> rows(ng);
+  int64_t next = 0;
+  for (int e = 0; e < ng; ++e) {
+    const GroupSpec& G = gs[e];
+    if (G.rows < 0 || G.row0 != next) return AVERIS_ERR_INVALID_ARG;
+    next += G.rows;
+    rows[e] = G.rows;
+    if (G.rows == 0) continue;
+    if (G.out_row != nullptr && !nvfp4_ok(G.out_row, G.rows, C)) return AVERIS_ERR_INVALID_ARG;
+    if (G.out_col != nullptr && !nvfp4_ok(G.out_col, C, G.rows)) return AVERIS_ERR_INVALID_ARG;
+    if (split && (G.mu == nullptr || G.mu_hat == nullptr || !aligned(G.mu, 16) || !aligned(G.mu_hat, 16) ||
+                  !nvfp4_ok(G.mu_q, 1, C)))
+      return AVERIS_ERR_INVALID_ARG;
+    if ((G.r_w == nullptr) != (G.r_out == nullptr)) return AVERIS_ERR_INVALID_ARG;
+    if (G.r_w != nullptr && (!split || G.r_w->rows < 1 || !nvfp4_ok(G.r_w, G.r_w->rows, C) || !aligned(G.r_out, 4)))
+      return AVERIS_ERR_INVALID_ARG;
+  }
+  if (next != L) return AVERIS_ERR_INVALID_ARG;
+  if (ws == nullptr || !aligned(ws, 256)) return AVERIS_ERR_INVALID_ARG;
+  if (ws_bytes < grouped_quant_ws_bytes(rows.data(), ng, C)) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
+  DeviceInfo* dev = nullptr;
+  averis_status st = device_info(&dev);
+  if (st != AVERIS_OK) return st;
+  const GroupedGeom geo = grouped_geom(L, C, std::min(ng, kMaxGroups));
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  for (int e0 = 0; e0 < ng; e0 += kMaxGroups) {
+    const int cnt = std::min(kMaxGroups, ng - e0);
+    if ((st = grouped_quantize_chunk(x, L, C, flags, gs + e0, cnt, geo, w, dev, s)) != AVERIS_OK) return st;
+    for (int e = e0; e < e0 + cnt; ++e)
+      if (rows[e] > 0) w += group_ctrl_bytes(geo) + group_part_bytes(geo, rows[e], C);
+  }
+  return AVERIS_OK;
+}
+
 // ----------------------------------------------------------------- GEMM --
 
 
-// early_start: the kernel launched just before this GEMM produced none of its
-// inputs (see GemmParams::early_start).
-averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const float* col_add, const float* row_vec,
-                        const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s,
-                        bool early_start = false) {
-  if (a == nullptr || b == nullptr || out == nullptr) return AVERIS_ERR_INVALID_ARG;
+// One GEMM of a launch: the operands and epilogue terms of averis_gemm.
+struct GemmSpec {
+  const averis_nvfp4* a = nullptr;
+  const averis_nvfp4* b = nullptr;
+  const float* col_add = nullptr;
+  const float* row_vec = nullptr;
+  const float* col_vec = nullptr;
+  float outer = 0.f;
+  void* out = nullptr;
+  int64_t ldo = 0;
+};
+
+// Argument checks of one GEMM (before anything touches the device).
+averis_status gemm_check(const GemmSpec& g, bool bf16) {
+  const averis_nvfp4* a = g.a;
+  const averis_nvfp4* b = g.b;
+  if (a == nullptr || b == nullptr || g.out == nullptr) return AVERIS_ERR_INVALID_ARG;
   const int64_t M = a->rows, N = b->rows, K = a->cols;
   // K may be ragged (the token axis of dW): codes and scales are zero-padded to 64
   if (M < 1 || N < 1 || K < 1 || b->cols != K) return AVERIS_ERR_INVALID_ARG;
   if (M > (int64_t)1 << 30 || N > (int64_t)1 << 30 || K > (int64_t)1 << 30) return AVERIS_ERR_INVALID_ARG;
   if (!nvfp4_ok(a, M, K) || !nvfp4_ok(b, N, K)) return AVERIS_ERR_INVALID_ARG;
-  const bool bf16 = (flags & AVERIS_OUT_BF16) != 0;
   const int64_t esz = bf16 ? 2 : 4;
-  if (ldo < N || (ldo * esz) % 16 != 0 || !aligned(out, 16)) return AVERIS_ERR_INVALID_ARG;
-  if ((row_vec == nullptr) != (col_vec == nullptr)) return AVERIS_ERR_INVALID_ARG;
-  DeviceInfo* dev = nullptr;
-  averis_status st = device_info(&dev);
-  if (st != AVERIS_OK) return st;
+  if (g.ldo < N || (g.ldo * esz) % 16 != 0 || !aligned(g.out, 16)) return AVERIS_ERR_INVALID_ARG;
+  if ((g.row_vec == nullptr) != (g.col_vec == nullptr)) return AVERIS_ERR_INVALID_ARG;
+  return AVERIS_OK;
+}
 
-  using Cfg = GemmCfg;
-  constexpr int BN = Cfg::BN;
+// Fills one checked GEMM's tensor maps and scalars.
+averis_status gemm_fill(const GemmSpec& g, bool bf16, CUtensorMap* ta, CUtensorMap* tb, CUtensorMap* td,
+                        GemmGroup* gg) {
+  const averis_nvfp4* a = g.a;
+  const averis_nvfp4* b = g.b;
+  const int64_t M = a->rows, N = b->rows, K = a->cols;
+  const int64_t esz = bf16 ? 2 : 4;
+  using Cfg = GemmCfg<kSfbFull>;
   const int64_t ld = averis_nvfp4_ld(K);
-  CUtensorMap ta, tb, td;
-  if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->codes, (uint64_t)ld, (uint64_t)M, (uint64_t)ld, Cfg::BKB,
+  if (!encode_2d(ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a->codes, (uint64_t)ld, (uint64_t)M, (uint64_t)ld, Cfg::BKB,
                  Cfg::BM))
     return AVERIS_ERR_CUDA;
-  if (!encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b->codes, (uint64_t)ld, (uint64_t)N, (uint64_t)ld, Cfg::BKB,
-                 BN))
+  if (!encode_2d(tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, b->codes, (uint64_t)ld, (uint64_t)N, (uint64_t)ld, Cfg::BKB,
+                 Cfg::BNH))
     return AVERIS_ERR_CUDA;
-  if (!encode_2d(&td, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, out, (uint64_t)N,
-                 (uint64_t)M, (uint64_t)(ldo * esz), bf16 ? 64u : 32u, 32u))
+  if (!encode_2d(td, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, g.out, (uint64_t)N,
+                 (uint64_t)M, (uint64_t)(g.ldo * esz), bf16 ? 64u : 32u, 32u))
     return AVERIS_ERR_CUDA;
+  gg->sfa = a->scales;
+  gg->sfb = b->scales;
+  gg->ts_a = a->tensor_scale;
+  gg->ts_b = b->tensor_scale;
+  gg->col_add = g.col_add;
+  gg->row_vec = g.row_vec;
+  gg->col_vec = g.col_vec;
+  gg->outer = g.outer;
+  gg->M = (int)M;
+  gg->N = (int)N;
+  gg->kc = (int)cdiv(K, 64);
+  gg->rb_a = (int)cdiv(M, 128);
+  gg->rb_b = (int)cdiv(N, 128);
+  gg->num_m = (int)cdiv(M, Cfg::PM);
+  return AVERIS_OK;
+}
 
-  GemmParams p{};
-  p.M = (int)M;
-  p.N = (int)N;
-  p.K = (int)K;
-  p.kc = (int)cdiv(K, 64);
-  p.rb_b = (int)cdiv(N, 128);
-  p.sfa = a->scales;
-  p.sfb = b->scales;
-  p.ts_a = a->tensor_scale;
-  p.ts_b = b->tensor_scale;
-  p.col_add = col_add;
-  p.row_vec = row_vec;
-  p.col_vec = col_vec;
-  p.outer = outer;
-  p.err = dev->err_word;
-  p.early_start = early_start ? 1 : 0;
-  const int64_t ntiles = cdiv(M, Cfg::BM) * cdiv(N, BN);
-  const int grid = (int)std::min<int64_t>(ntiles, dev->sms);
-  cudaError_t e = bf16 ? launch_pdl(gemm_nvfp4_kernel<true>, dim3(grid), dim3(kGemmThreads), Cfg::SMEM, s, ta, tb, td, p)
-                       : launch_pdl(gemm_nvfp4_kernel<false>, dim3(grid), dim3(kGemmThreads), Cfg::SMEM, s, ta, tb, td, p);
+// Up to G GEMMs (same output type) in one persistent launch of CTA pairs.
+// early_start: the kernel launched just before produced none of their inputs
+// (see GemmArgs::early_start).  splits > 1 (one binary32 GEMM only): split K
+// with partials in `part` and tickets in `tickets` (zero at rest).
+template <int G>
+averis_status gemm_launch(const GemmSpec* specs, int n, unsigned flags, cudaStream_t s, bool early_start,
+                          int splits = 1, float* part = nullptr, unsigned* tickets = nullptr) {
+  if (n < 1 || n > G) return AVERIS_ERR_INVALID_ARG;
+  const bool bf16 = (flags & AVERIS_OUT_BF16) != 0;
+  if (splits > 1 && (G != 1 || bf16 || part == nullptr || tickets == nullptr)) return AVERIS_ERR_INVALID_ARG;
+  averis_status st = AVERIS_OK;
+  for (int e = 0; e < n; ++e)
+    if ((st = gemm_check(specs[e], bf16)) != AVERIS_OK) return st;
+  DeviceInfo* dev = nullptr;
+  if ((st = device_info(&dev)) != AVERIS_OK) return st;
+  using Cfg = GemmCfg<kSfbFull>;
+  static thread_local GemmArgs<G> args;  // about 30 KB for G = 64: kept off the stack
+  std::memset(&args, 0, sizeof(args));
+  args.splits = splits > 1 ? splits : 1;
+  int64_t units = 0;
+  for (int e = 0; e < n; ++e) {
+    if ((st = gemm_fill(specs[e], bf16, &args.tmA[e], &args.tmB[e], &args.tmD[e], &args.g[e])) != AVERIS_OK)
+      return st;
+    args.g[e].unit0 = (int)units;
+    units += (int64_t)args.g[e].num_m * cdiv(args.g[e].N, Cfg::BN) * args.splits;
+    if (units > (int64_t)1 << 30) return AVERIS_ERR_INVALID_ARG;
+  }
+  args.ngroups = n;
+  args.nunits = (int)units;
+  args.err = dev->err_word;
+  args.wait_limit = kWaitLimit;
+  args.early_start = early_start ? 1 : 0;
+  args.part = part;
+  args.tickets = tickets;
+  // pairs of CTAs (clusters of two), at most the pairs resident at once
+  const int grid = 2 * (int)std::min<int64_t>(units, dev->gemm_pairs);
+  cudaError_t e = bf16 ? launch_pdl(gemm_nvfp4_kernel<true, kSfbFull, G>, dim3(grid), dim3(kGemmThreads), Cfg::SMEM,
+                                    s, args)
+                       : launch_pdl(gemm_nvfp4_kernel<false, kSfbFull, G>, dim3(grid), dim3(kGemmThreads),
+                                    Cfg::SMEM, s, args);
   return e == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA;
+}
+
+averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const float* col_add, const float* row_vec,
+                        const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s,
+                        bool early_start = false, int splits = 1, float* part = nullptr, unsigned* tickets = nullptr) {
+  GemmSpec g;
+  g.a = a;
+  g.b = b;
+  g.col_add = col_add;
+  g.row_vec = row_vec;
+  g.col_vec = col_vec;
+  g.outer = outer;
+  g.out = out;
+  g.ldo = ldo;
+  return gemm_launch<1>(&g, 1, flags, s, early_start, splits, part, tickets);
+}
+
+// Many GEMMs (same output type), kMaxGemmGroups per launch.
+averis_status grouped_gemm_impl(const GemmSpec* specs, int n, unsigned flags, cudaStream_t s, bool early_start) {
+  for (int e0 = 0; e0 < n; e0 += kMaxGemmGroups) {
+    const int cnt = std::min(kMaxGemmGroups, n - e0);
+    const averis_status st = gemm_launch<kMaxGemmGroups>(specs + e0, cnt, flags, s, early_start && e0 == 0);
+    if (st != AVERIS_OK) return st;
+  }
+  return AVERIS_OK;
 }
 
 averis_status rank1_impl(const averis_nvfp4* mu_q, const averis_nvfp4* w, float* out, cudaStream_t s) {
@@ -424,9 +751,38 @@ averis_nvfp4 carve_nvfp4(Carver& c, int64_t rows, int64_t cols) {
 
 size_t fwd_ws(int64_t l, int64_t m, int64_t n) { return quant_ws_bytes(l, m) + align256((size_t)n * 4); }
 
+// Split K of the weight-gradient GEMM (M = m, N = n, K = l): how many K
+// ranges each 256 x 256 tile is cut into.  Chosen from the shape alone (with
+// the pair count of a 148-SM B300), so that the workspace size does not
+// depend on the device: the fewest ranges whose modelled time -- waves of
+// units times (K tiles per range + epilogue, + partial traffic when split)
+// -- is clearly the shortest, with at least four K tiles per range.
+constexpr int64_t kNominalPairs = 74;
+int dw_splits(int64_t M, int64_t N, int64_t K) {
+  const int64_t tiles = cdiv(M, 256) * cdiv(N, 256);
+  const int64_t nkt = cdiv(cdiv(K, 64), 4);
+  if (tiles * 2 > kMaxGemmTickets) return 1;  // its tickets live in the workspace's control block
+  int best = 1;
+  double best_t = 0.0;
+  for (int S = 1; S <= 4; ++S) {
+    if (S > 1 && nkt < 4 * S) break;
+    const double t = (double)cdiv(tiles * S, kNominalPairs) * ((double)cdiv(nkt, S) + 2.0 + (S > 1 ? 2.0 : 0.0));
+    if (S == 1 || t < 0.9 * best_t) {
+      best = S;
+      best_t = t;
+    }
+  }
+  return best;
+}
+size_t dw_split_part_bytes(int64_t M, int64_t N, int64_t K) {
+  const int S = dw_splits(M, N, K);
+  if (S == 1) return 0;
+  return align256((size_t)cdiv(M, 256) * cdiv(N, 256) * S * 2 * 256 * 128 * sizeof(float));
+}
+
 size_t bwd_ws(int64_t l, int64_t m, int64_t n) {
   return quant_ws_bytes(l, n) + nvfp4_bytes(l, n) + nvfp4_bytes(n, l) + nvfp4_bytes(1, n) +
-         2 * align256((size_t)n * 4) + align256((size_t)m * 4);
+         2 * align256((size_t)n * 4) + align256((size_t)m * 4) + dw_split_part_bytes(m, n, l);
 }
 
 averis_status linear_fwd_impl(const void* x, int64_t l, int64_t m, int64_t n, const averis_nvfp4* w_m, unsigned flags,
@@ -464,6 +820,10 @@ averis_status linear_bwd_impl(const void* d, int64_t l, int64_t m, int64_t n, co
   float* mu = static_cast<float*>(c.take((size_t)n * 4));
   float* mu_hat = static_cast<float*>(c.take((size_t)n * 4));
   float* r_d = static_cast<float*>(c.take((size_t)m * 4));
+  const int splits = dw_splits(m, n, l);
+  // the tickets sit in the control block at the workspace's head (zero at rest for every shape)
+  unsigned* tickets = splits > 1 ? static_cast<unsigned*>(qws) + kCtrlGemmTicket : nullptr;
+  float* part = splits > 1 ? static_cast<float*>(c.take(dw_split_part_bytes(m, n, l))) : nullptr;
   averis_status r = quantize_impl(d, l, n, flags, mu, &mu_q, mu_hat, &d_row, &d_col, qws, quant_ws_bytes(l, n), s,
                                   split ? w_n : nullptr, split ? r_d : nullptr);
   if (r != AVERIS_OK) return r;
@@ -472,7 +832,7 @@ averis_status linear_bwd_impl(const void* d, int64_t l, int64_t m, int64_t n, co
   // dW reads the forward state and D's quantized column layout, not dX: it
   // starts while the input-gradient GEMM drains
   return gemm_impl(&st->x_col, &d_col, nullptr, split ? st->mu_hat : nullptr, split ? mu_hat : nullptr, (float)l, dw,
-                   n, flags & ~AVERIS_OUT_BF16, s, /*early_start=*/true);
+                   n, flags & ~AVERIS_OUT_BF16, s, /*early_start=*/true, splits, part, tickets);
 }
 
 // Zeroes the control block of the allocation-free call's scratch on this
@@ -568,34 +928,51 @@ averis_status nvfp4_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n, c
 // ------------------------------------------------------- grouped (MoE) --
 
 static bool offsets_ok(const int64_t* offsets, int64_t num_experts) {
-  if (offsets == nullptr || num_experts < 1 || offsets[0] != 0) return false;
+  if (offsets == nullptr || num_experts < 1 || num_experts > (1 << 20) || offsets[0] != 0) return false;
   for (int64_t e = 0; e < num_experts; ++e)
     if (offsets[e + 1] < offsets[e]) return false;
   return true;
+}
+
+static std::vector<int64_t> group_rows(const int64_t* offsets, int64_t num_experts) {
+  std::vector<int64_t> r((size_t)num_experts);
+  for (int64_t e = 0; e < num_experts; ++e) r[(size_t)e] = offsets[e + 1] - offsets[e];
+  return r;
+}
+
+// Forward workspace: the grouped quantize's control words and partials, then
+// one rank-one row [n] per expert.
+static size_t grouped_fwd_ws(const int64_t* offsets, int64_t E, int64_t m, int64_t n) {
+  const std::vector<int64_t> rows = group_rows(offsets, E);
+  return align256(grouped_quant_ws_bytes(rows.data(), (int)E, m)) + (size_t)E * align256((size_t)n * 4);
+}
+
+// Backward workspace: the grouped quantize's, then per expert with rows its
+// quantized D (both layouts), mean, NVFP4 mean, dequantized mean and rank-one row [m].
+static size_t grouped_bwd_ws(const int64_t* offsets, int64_t E, int64_t m, int64_t n) {
+  const std::vector<int64_t> rows = group_rows(offsets, E);
+  size_t b = align256(grouped_quant_ws_bytes(rows.data(), (int)E, n));
+  for (int64_t e = 0; e < E; ++e) {
+    const int64_t le = rows[(size_t)e];
+    if (le > 0)
+      b += nvfp4_bytes(le, n) + nvfp4_bytes(n, le) + nvfp4_bytes(1, n) + 2 * align256((size_t)n * 4) +
+           align256((size_t)m * 4);
+  }
+  return b;
 }
 
 size_t averis_grouped_linear_fwd_workspace_bytes(const int64_t* offsets, int64_t num_experts, int64_t m, int64_t n,
                                                  unsigned flags) {
   (void)flags;
   if (!offsets_ok(offsets, num_experts) || m < 1 || n < 1) return 0;
-  size_t b = 0;
-  for (int64_t e = 0; e < num_experts; ++e) {
-    const int64_t le = offsets[e + 1] - offsets[e];
-    if (le > 0) b = std::max(b, fwd_ws(le, m, n));
-  }
-  return std::max<size_t>(b, 256);
+  return grouped_fwd_ws(offsets, num_experts, m, n);
 }
 
 size_t averis_grouped_linear_bwd_workspace_bytes(const int64_t* offsets, int64_t num_experts, int64_t m, int64_t n,
                                                  unsigned flags) {
   (void)flags;
   if (!offsets_ok(offsets, num_experts) || m < 1 || n < 1) return 0;
-  size_t b = 0;
-  for (int64_t e = 0; e < num_experts; ++e) {
-    const int64_t le = offsets[e + 1] - offsets[e];
-    if (le > 0) b = std::max(b, bwd_ws(le, m, n));
-  }
-  return std::max<size_t>(b, 256);
+  return grouped_bwd_ws(offsets, num_experts, m, n);
 }
 
 averis_status averis_grouped_linear_fwd(const void* x, const int64_t* offsets, int64_t num_experts, int64_t m,
@@ -604,16 +981,52 @@ averis_status averis_grouped_linear_fwd(const void* x, const int64_t* offsets, i
                                         cudaStream_t stream) {
   if (x == nullptr || y == nullptr || w_m == nullptr || states == nullptr) return AVERIS_ERR_INVALID_ARG;
   if (!offsets_ok(offsets, num_experts)) return AVERIS_ERR_INVALID_ARG;
-  const int64_t esz = (flags & AVERIS_OUT_BF16) ? 2 : 4;
-  for (int64_t e = 0; e < num_experts; ++e) {
-    const int64_t r0 = offsets[e], le = offsets[e + 1] - offsets[e];
-    if (le == 0) continue;
-    const averis_status st = linear_fwd_impl(static_cast<const uint8_t*>(x) + r0 * m * 2, le, m, n, &w_m[e], flags,
-                                             static_cast<uint8_t*>(y) + r0 * n * esz, &states[e], workspace,
-                                             workspace_bytes, stream);
-    if (st != AVERIS_OK) return st;
+  if (m < 16 || n < 16 || m % 16 || n % 16) return AVERIS_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256)) return AVERIS_ERR_INVALID_ARG;
+  if (workspace_bytes < grouped_fwd_ws(offsets, num_experts, m, n)) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
+  const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
+  const int64_t E = num_experts, L = offsets[E];
+  if (L < 1) return AVERIS_OK;
+  for (int64_t e = 0; e < E; ++e)
+    if (offsets[e + 1] > offsets[e] && !nvfp4_ok(&w_m[e], n, m)) return AVERIS_ERR_INVALID_ARG;
+  const std::vector<int64_t> rows = group_rows(offsets, E);
+  Carver c(workspace);
+  void* qws = c.take(grouped_quant_ws_bytes(rows.data(), (int)E, m));
+  std::vector<GroupSpec> gs((size_t)E);
+  std::vector<float*> r_x((size_t)E);
+  for (int64_t e = 0; e < E; ++e) {
+    r_x[(size_t)e] = static_cast<float*>(c.take((size_t)n * 4));
+    GroupSpec& G = gs[(size_t)e];
+    G.row0 = offsets[e];
+    G.rows = rows[(size_t)e];
+    if (G.rows == 0) continue;
+    const averis_fwd_state& st = states[e];
+    G.mu = st.mu;
+    G.mu_q = &st.mu_q;
+    G.mu_hat = st.mu_hat;
+    G.out_row = &st.x_row;
+    G.out_col = &st.x_col;
+    if (split) {
+      G.r_w = &w_m[e];
+      G.r_out = r_x[(size_t)e];
+    }
   }
-  return AVERIS_OK;
+  averis_status r = grouped_quantize_impl(x, L, m, flags, gs.data(), (int)E, qws,
+                                          grouped_quant_ws_bytes(rows.data(), (int)E, m), stream);
+  if (r != AVERIS_OK) return r;
+  const int64_t esz = (flags & AVERIS_OUT_BF16) ? 2 : 4;
+  std::vector<GemmSpec> gm;
+  for (int64_t e = 0; e < E; ++e) {
+    if (rows[(size_t)e] == 0) continue;
+    GemmSpec g;
+    g.a = &states[e].x_row;
+    g.b = &w_m[e];
+    g.col_add = split ? r_x[(size_t)e] : nullptr;
+    g.out = static_cast<uint8_t*>(y) + offsets[e] * n * esz;
+    g.ldo = n;
+    gm.push_back(g);
+  }
+  return grouped_gemm_impl(gm.data(), (int)gm.size(), flags, stream, false);
 }
 
 averis_status averis_grouped_linear_bwd(const void* d, const int64_t* offsets, int64_t num_experts, int64_t m,
@@ -623,16 +1036,80 @@ averis_status averis_grouped_linear_bwd(const void* d, const int64_t* offsets, i
   if (d == nullptr || dx == nullptr || dw == nullptr || w_n == nullptr || states == nullptr)
     return AVERIS_ERR_INVALID_ARG;
   if (!offsets_ok(offsets, num_experts)) return AVERIS_ERR_INVALID_ARG;
-  const int64_t esz = (flags & AVERIS_OUT_BF16) ? 2 : 4;
-  for (int64_t e = 0; e < num_experts; ++e) {
-    const int64_t r0 = offsets[e], le = offsets[e + 1] - offsets[e];
+  if (m < 16 || n < 16 || m % 16 || n % 16) return AVERIS_ERR_INVALID_ARG;
+  if (workspace == nullptr || !aligned(workspace, 256)) return AVERIS_ERR_INVALID_ARG;
+  if (workspace_bytes < grouped_bwd_ws(offsets, num_experts, m, n)) return AVERIS_ERR_WORKSPACE_TOO_SMALL;
+  const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
+  const int64_t E = num_experts, L = offsets[E];
+  if (L < 1) return AVERIS_OK;
+  for (int64_t e = 0; e < E; ++e) {
+    const int64_t le = offsets[e + 1] - offsets[e];
     if (le == 0) continue;
-    const averis_status st = linear_bwd_impl(static_cast<const uint8_t*>(d) + r0 * n * 2, le, m, n, &states[e],
-                                             &w_n[e], flags, static_cast<uint8_t*>(dx) + r0 * m * esz, dw[e],
-                                             workspace, workspace_bytes, stream);
-    if (st != AVERIS_OK) return st;
+    if (!nvfp4_ok(&w_n[e], m, n) || !nvfp4_ok(&states[e].x_col, m, le) || dw[e] == nullptr)
+      return AVERIS_ERR_INVALID_ARG;
+    if (split && states[e].mu_hat == nullptr) return AVERIS_ERR_INVALID_ARG;
   }
-  return AVERIS_OK;
+  const std::vector<int64_t> rows = group_rows(offsets, E);
+  Carver c(workspace);
+  void* qws = c.take(grouped_quant_ws_bytes(rows.data(), (int)E, n));
+  struct DState {
+    averis_nvfp4 row, col, mu_q;
+    float *mu, *mu_hat, *r_d;
+  };
+  std::vector<DState> ds((size_t)E);
+  std::vector<GroupSpec> gs((size_t)E);
+  for (int64_t e = 0; e < E; ++e) {
+    const int64_t le = rows[(size_t)e];
+    GroupSpec& G = gs[(size_t)e];
+    G.row0 = offsets[e];
+    G.rows = le;
+    if (le == 0) continue;
+    DState& D = ds[(size_t)e];
+    D.row = carve_nvfp4(c, le, n);
+    D.col = carve_nvfp4(c, n, le);
+    D.mu_q = carve_nvfp4(c, 1, n);
+    D.mu = static_cast<float*>(c.take((size_t)n * 4));
+    D.mu_hat = static_cast<float*>(c.take((size_t)n * 4));
+    D.r_d = static_cast<float*>(c.take((size_t)m * 4));
+    G.mu = D.mu;
+    G.mu_q = &D.mu_q;
+    G.mu_hat = D.mu_hat;
+    G.out_row = &D.row;
+    G.out_col = &D.col;
+    if (split) {
+      G.r_w = &w_n[e];
+      G.r_out = D.r_d;
+    }
+  }
+  averis_status r = grouped_quantize_impl(d, L, n, flags, gs.data(), (int)E, qws,
+                                          grouped_quant_ws_bytes(rows.data(), (int)E, n), stream);
+  if (r != AVERIS_OK) return r;
+  const int64_t esz = (flags & AVERIS_OUT_BF16) ? 2 : 4;
+  std::vector<GemmSpec> gx, gw;
+  for (int64_t e = 0; e < E; ++e) {
+    const int64_t le = rows[(size_t)e];
+    if (le == 0) continue;
+    const DState& D = ds[(size_t)e];
+    GemmSpec a;
+    a.a = &D.row;
+    a.b = &w_n[e];
+    a.col_add = split ? D.r_d : nullptr;
+    a.out = static_cast<uint8_t*>(dx) + offsets[e] * m * esz;
+    a.ldo = m;
+    gx.push_back(a);
+    GemmSpec w;
+    w.a = &states[e].x_col;
+    w.b = &D.col;
+    w.row_vec = split ? states[e].mu_hat : nullptr;
+    w.col_vec = split ? D.mu_hat : nullptr;
+    w.outer = (float)le;
+    w.out = dw[e];
+    w.ldo = n;
+    gw.push_back(w);
+  }
+  if ((r = grouped_gemm_impl(gx.data(), (int)gx.size(), flags, stream, false)) != AVERIS_OK) return r;
+  // the weight gradients read the forward states and D's column layouts, not dX
+  return grouped_gemm_impl(gw.data(), (int)gw.size(), flags & ~AVERIS_OUT_BF16, stream, true);
 }
 
 const char* averis_status_string(averis_status status) {
@@ -673,7 +1150,7 @@ averis_status averis_debug_starve_next_quantize(long long wait_cycles) {
   return AVERIS_OK;
 }
 
-int averis_version(void) { return 100; }
+int averis_version(void) { return 20000; }
 
 }  // extern "C"
 

@@ -41,7 +41,9 @@ enum : int {
   kCtrlQuantTicket = 7,  // quantize pass: CTAs finished
   kCtrlStrip = 64,       // per-strip-group tickets of the stats pass
   kMaxStripGroups = 1024,
-  kCtrlWords = kCtrlStrip + kMaxStripGroups
+  kCtrlGemmTicket = kCtrlStrip + kMaxStripGroups,  // split-K tickets of a GEMM sharing the workspace
+  kMaxGemmTickets = 2048,
+  kCtrlWords = kCtrlGemmTicket + kMaxGemmTickets
 };
 
 struct ColPartial {
@@ -232,6 +234,7 @@ struct StatsParams {
   // diagnostics only: issue no input loads, so that every wait for a box runs
   // out (exercises the timeout path with no copy in flight)
   int starve;
+  int64_t row_base;   // first row of these R rows in the tensor map (a group of a grouped input)
 };
 
 // Column statistics in one pass over X, with the combine fused in.
@@ -252,7 +255,9 @@ constexpr int kStatsBufs = 3;                                 // boxes in flight
 constexpr int kStatsBox = kStatsBoxRows * 128;                // 64 bf16 columns x 256 rows (32 KB)
 constexpr int kStatsSmem = kStatsBufs * kStatsBox + 1024;     // + alignment slack for the 128-byte swizzle
 
-__global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant__ CUtensorMap tmX, StatsParams p) {
+// The pass of one CTA: strip group bx of nbx, row block by of nby.
+__device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const StatsParams& p, int bx, int nbx, int by,
+                                              int nby) {
   extern __shared__ uint8_t stats_raw[];
   uint8_t* ring = stats_raw + ((1024u - (ptx::smem_u32(stats_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
   __shared__ F2 s_sum[8][64];
@@ -273,11 +278,11 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g8 = tid & 7;     // 8-column group inside the strip
   const int rl = tid >> 3;    // row lane 0..31
-  const int64_t rb0 = (int64_t)blockIdx.y * p.rows_per;
+  const int64_t rb0 = (int64_t)by * p.rows_per;
   const int64_t rb1 = min(p.R, rb0 + p.rows_per);
 
   bool failed = false;  // a box never arrived (uniform over the CTA)
-  for (int strip = blockIdx.x; strip < p.nstrips && !failed; strip += gridDim.x) {
+  for (int strip = bx; strip < p.nstrips && !failed; strip += nbx) {
     // column pairs (2w, 2w+1): Kahan-compensated binary32 sums, packed bf16 max / min
     uint64_t s2[4], c2[4];
     uint32_t mx2[4], mn2[4];
@@ -322,7 +327,8 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
       for (int64_t k = 0; k < kStatsBufs && k < nbox; ++k) {
         const uint32_t b = (it + (uint32_t)k) % kStatsBufs;
         ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
-        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64, (int32_t)(rb0 + k * kStatsBoxRows), &s_full[b]);
+        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64, (int32_t)(p.row_base + rb0 + k * kStatsBoxRows),
+                         &s_full[b]);
       }
     for (int64_t k = 0; k < nbox; ++k, ++it) {
       const uint32_t b = it % kStatsBufs;
@@ -364,8 +370,8 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
       __syncthreads();  // the buffer is free
       if (threadIdx.x == 0 && k + kStatsBufs < nbox) {
         ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
-        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64, (int32_t)(rb0 + (k + kStatsBufs) * kStatsBoxRows),
-                         &s_full[b]);
+        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64,
+                         (int32_t)(p.row_base + rb0 + (k + kStatsBufs) * kStatsBoxRows), &s_full[b]);
       }
     }
     if (failed) break;
@@ -405,7 +411,7 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
         m2 = fminf(m2, s_mn[w][tid]);
       }
       if (col < p.C)
-        *reinterpret_cast<float4*>(p.part + (int64_t)blockIdx.y * p.C + col) = make_float4(acc.hi, acc.lo, m1, m2);
+        *reinterpret_cast<float4*>(p.part + (int64_t)by * p.C + col) = make_float4(acc.hi, acc.lo, m1, m2);
     }
     __syncthreads();
   }
@@ -414,17 +420,17 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const unsigned t = atomicAdd(&p.ctrl[kCtrlStrip + blockIdx.x], 1u);
-    s_last = (t == gridDim.y - 1);
+    const unsigned t = atomicAdd(&p.ctrl[kCtrlStrip + bx], 1u);
+    s_last = (t == (unsigned)nby - 1);
   }
   __syncthreads();
   if (!s_last) return;
   __threadfence();
 
   float a_res = 0.f;
-  const int nrb = (int)gridDim.y;
+  const int nrb = nby;
   const float Rf = (float)p.R;
-  for (int strip = blockIdx.x; strip < p.nstrips; strip += gridDim.x) {
+  for (int strip = bx; strip < p.nstrips; strip += nbx) {
     const int cl = tid & 63, part = tid >> 6;
     const int64_t col = (int64_t)strip * 64 + cl;
     F2 acc{0.f, 0.f};
@@ -463,9 +469,33 @@ __global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant_
     }
     __syncthreads();
   }
-  if (tid == 0) p.ctrl[kCtrlStrip + blockIdx.x] = 0u;  // every row block has arrived: reset for the next call
+  if (tid == 0) p.ctrl[kCtrlStrip + bx] = 0u;  // every row block has arrived: reset for the next call
   a_res = block_max256(a_res, red);
   if (tid == 0) atomicMax(&p.ctrl[kCtrlAmaxRes], __float_as_uint(a_res));
+}
+
+__global__ void __launch_bounds__(256, 2) colstats_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                          const __grid_constant__ StatsParams p) {
+  colstats_body(tmX, p, blockIdx.x, gridDim.x, blockIdx.y, gridDim.y);
+}
+
+// Groups (experts) of a grouped input, one launch: at most kMaxGroups per launch.
+constexpr int kMaxGroups = 64;
+
+// The stats pass over the row groups of a grouped input: group e owns row
+// blocks rb0[e] .. rb0[e+1]-1 of the grid's y dimension; g[e] holds its rows,
+// partials, control words and mean.
+struct GroupedStatsParams {
+  StatsParams g[kMaxGroups];
+  int rb0[kMaxGroups + 1];
+  int ngroups;
+};
+
+__global__ void __launch_bounds__(256, 2) colstats_grouped_kernel(const __grid_constant__ CUtensorMap tmX,
+                                                                  const __grid_constant__ GroupedStatsParams gp) {
+  int e = 0;
+  while (e + 1 < gp.ngroups && gp.rb0[e + 1] <= (int)blockIdx.y) ++e;
+  colstats_body(tmX, gp.g[e], blockIdx.x, gridDim.x, (int)blockIdx.y - gp.rb0[e], gp.rb0[e + 1] - gp.rb0[e]);
 }
 
 // NVFP4 of the mean as one [1, C] row, into SMEM (codes: C/2 bytes, one E4M3
@@ -645,6 +675,7 @@ struct QuantParams {
   // rest quantize tiles
   int mean_ctas;
   long long wait_limit;  // bound of every wait, in SM clock cycles
+  int64_t row_base;      // first row of these R rows in the tensor map (a group of a grouped input)
   // optional rank-one row (split only): r[N] = deq(mu_q) deq(W)^T, with W an
   // NVFP4 [N, C] tensor blocked along C (the blocking of the mean)
   const uint8_t* w_codes;
@@ -834,9 +865,9 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
 // CTA to finish resets the control block's maxima.  AMAX_ONLY: compute the
 // rotated residual's per-layout maximum magnitude (Hadamard variant)
 // instead of quantizing.
+// The pass of CTA `cta` of the `ncta` CTAs given to one tensor (or group).
 template <bool AMAX_ONLY, bool HAD>
-__global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
-    split_quant_kernel(const __grid_constant__ CUtensorMap tmX, const QuantParams p) {
+__device__ __forceinline__ void split_quant_body(const CUtensorMap& tmX, const QuantParams& p, int cta, int ncta) {
   extern __shared__ uint8_t qraw[];
   uint8_t* sm = qraw + ((1024u - (ptx::smem_u32(qraw) & 1023u)) & 1023u);  // stays a shared-space pointer
   float* mu_s = reinterpret_cast<float*>(sm + kQOffMu);
@@ -848,8 +879,8 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
   const int tid = threadIdx.x, lane = tid & 31;
   const int ntiles = p.tiles_r * p.tiles_c;
   const bool split = p.mu != nullptr;
-  const bool mean_cta = (int)blockIdx.x < p.mean_ctas;
-  const int tcta = (int)blockIdx.x - p.mean_ctas, ntcta = (int)gridDim.x - p.mean_ctas;  // tile CTA index, count
+  const bool mean_cta = cta < p.mean_ctas;
+  const int tcta = cta - p.mean_ctas, ntcta = ncta - p.mean_ctas;  // tile CTA index, count
   const bool rows_on = AMAX_ONLY || p.row_codes != nullptr;
   const bool cols_on = AMAX_ONLY || p.col_codes != nullptr;
 
@@ -860,8 +891,9 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
   auto issue_x = [&](int tile, int b) {
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     ptx::mbar_arrive_expect_tx(&full[b], (uint32_t)kQTileBytes + (split ? mu_bytes(tile) : 0u));
-    ptx::tma_load_2d(sm + b * kQTileBytes, &tmX, tc * kQTile, tr * kQTile, &full[b]);
-    ptx::tma_load_2d(sm + b * kQTileBytes + kQHalf, &tmX, tc * kQTile + 64, tr * kQTile, &full[b]);
+    const int32_t y = (int32_t)(p.row_base + (int64_t)tr * kQTile);
+    ptx::tma_load_2d(sm + b * kQTileBytes, &tmX, tc * kQTile, y, &full[b]);
+    ptx::tma_load_2d(sm + b * kQTileBytes + kQHalf, &tmX, tc * kQTile + 64, y, &full[b]);
   };
   auto issue_mu = [&](int tile, int b) {
     if (split) ptx::bulk_load(mu_s + 128 * b, p.mu + (int64_t)(tile % p.tiles_c) * kQTile, mu_bytes(tile), &full[b]);
@@ -892,7 +924,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
       inv_s[tid] = tid < 127 ? inv_scale_of(tid, s_row) : 0.f;
       inv_s[128 + tid] = tid < 127 ? inv_scale_of(tid, s_col) : 0.f;
     }
-    if (blockIdx.x == 0 && tid == 0) {
+    if (cta == 0 && tid == 0) {
       if (p.row_ts) *p.row_ts = s_row;
       if (p.col_ts) *p.col_ts = s_col;
     }
@@ -904,10 +936,10 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     // the mean as NVFP4 (CTA 0 writes it out) and this CTA's share of the rank-one row
     uint8_t* s_codes = sm;                        // tile buffers are unused in a mean CTA
     uint8_t* s_scales = sm + kQOffMu - kQBufs * kQTileBytes / 4;
-    const float s_mu = quantize_mean(p, blockIdx.x == 0, s_codes, s_scales, red);
+    const float s_mu = quantize_mean(p, cta == 0, s_codes, s_scales, red);
     if (p.r_out != nullptr) {
       const int64_t per = (p.w_rows + p.mean_ctas - 1) / p.mean_ctas;
-      const int64_t n0 = (int64_t)blockIdx.x * per;
+      const int64_t n0 = (int64_t)cta * per;
       rank1_rows(p, n0, min(p.w_rows, n0 + per), s_codes, s_scales, s_mu);
     }
   }
@@ -990,7 +1022,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     if (tid == 0) {
       __threadfence();
       const unsigned t = atomicAdd(&p.ctrl[kCtrlQuantTicket], 1u);
-      s_last = (t == gridDim.x - 1);
+      s_last = (t == (unsigned)ncta - 1);
       if (s_last) {
         p.ctrl[kCtrlAmaxRes] = 0u;
         p.ctrl[kCtrlAmaxRowH] = 0u;
@@ -999,6 +1031,33 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
       }
     }
   }
+}
+
+template <bool AMAX_ONLY, bool HAD>
+__global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
+    split_quant_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ QuantParams p) {
+  split_quant_body<AMAX_ONLY, HAD>(tmX, p, blockIdx.x, gridDim.x);
+}
+
+// The quantize pass over the row groups of a grouped input: group e owns CTAs
+// cta0[e] .. cta0[e+1]-1 (its mean CTAs first), g[e] its rows, outputs and
+// control words.
+struct GroupedQuantParams {
+  QuantParams g[kMaxGroups];
+  int cta0[kMaxGroups + 1];
+  int ngroups;
+};
+
+// kernel parameters are limited to 32764 bytes (with the tensor map)
+static_assert(sizeof(GroupedQuantParams) + sizeof(CUtensorMap) <= 32000, "grouped quantize parameters too large");
+static_assert(sizeof(GroupedStatsParams) + sizeof(CUtensorMap) <= 32000, "grouped stats parameters too large");
+
+template <bool AMAX_ONLY, bool HAD>
+__global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
+    split_quant_grouped_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ GroupedQuantParams gp) {
+  int e = 0;
+  while (e + 1 < gp.ngroups && gp.cta0[e + 1] <= (int)blockIdx.x) ++e;
+  split_quant_body<AMAX_ONLY, HAD>(tmX, gp.g[e], (int)blockIdx.x - gp.cta0[e], gp.cta0[e + 1] - gp.cta0[e]);
 }
 
 // --------------------------------------------------------- rank-one GEMV --
