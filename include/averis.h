@@ -75,6 +75,8 @@ typedef enum {
 
 /* Size of the control block at the head of every workspace (zero at rest). */
 #define AVERIS_WORKSPACE_CTRL_BYTES 12544
+/* The same for the workspaces of the grouped (mixture-of-experts) calls. */
+#define AVERIS_GROUPED_WORKSPACE_CTRL_BYTES 278528
 
 /* flags */
 #define AVERIS_MEAN_SPLIT 1u  /* subtract the column mean (Averis); clear = vanilla NVFP4 */
@@ -244,8 +246,12 @@ averis_status nvfp4_linear_bwd(const void* d, int64_t l, int64_t m, int64_t n,
  *  states        HOST array of E forward states, expert e's sized for its rows.
  *  y / dx        device [L, n] / [L, m], the rows grouped like x;  dw  HOST
  *                array of E device pointers to binary32 [m, n].
- *  workspace     averis_grouped_linear_*_workspace_bytes() bytes (reused by
- *                the experts in turn, which run one after another on `stream`).
+ *  workspace     averis_grouped_linear_*_workspace_bytes() bytes; its first
+ *                AVERIS_GROUPED_WORKSPACE_CTRL_BYTES bytes are its control
+ *                block (zero before first use, left zero by every call).
+ *                All experts are quantized together (one launch per pass for
+ *                up to 64 experts) and their GEMMs run in one persistent
+ *                launch per product (Y; dX; dW).
  *  flags         AVERIS_MEAN_SPLIT (clear: vanilla NVFP4), AVERIS_HADAMARD16,
  *                AVERIS_OUT_BF16.
  */

@@ -384,8 +384,13 @@ GroupedGeom grouped_geom(int64_t L, int64_t C, int ngroups) {
   g.rows_per = std::max<int64_t>(256, cdiv(cdiv(L, target), 32) * 32);
   return g;
 }
-// Per-group control words (strip tickets and maxima, zero at rest) and row-block partials.
-size_t group_ctrl_bytes(const GroupedGeom& g) { return align256((size_t)(kCtrlStrip + g.gx) * sizeof(unsigned)); }
+// Control words of the groups of one launch (strip tickets and maxima, zero at
+// rest): a fixed region at the head of every grouped workspace, the same for
+// every shape, so that a workspace can serve grouped calls of any shape (every
+// word of the region is zero between calls); then the groups' row-block partials.
+constexpr size_t kGroupCtrlWords = kCtrlStrip + kMaxStripGroups;
+static_assert(kMaxGroups * kGroupCtrlWords * sizeof(unsigned) == AVERIS_GROUPED_WORKSPACE_CTRL_BYTES,
+              "grouped control region is part of the ABI");
 size_t group_part_bytes(const GroupedGeom& g, int64_t rows, int64_t C) {
   return align256((size_t)cdiv(rows, g.rows_per) * (size_t)C * sizeof(ColPartial));
 }
@@ -393,18 +398,19 @@ size_t grouped_quant_ws_bytes(const int64_t* rows, int ng, int64_t C) {
   int64_t L = 0;
   for (int e = 0; e < ng; ++e) L += rows[e];
   const GroupedGeom g = grouped_geom(L, C, std::min(ng, kMaxGroups));
-  size_t b = 0;
+  size_t b = AVERIS_GROUPED_WORKSPACE_CTRL_BYTES;
   for (int e = 0; e < ng; ++e)
-    if (rows[e] > 0) b += group_ctrl_bytes(g) + group_part_bytes(g, rows[e], C);
-  return std::max<size_t>(b, 256);
+    if (rows[e] > 0) b += group_part_bytes(g, rows[e], C);
+  return b;
 }
 
 // The quantize pass of up to kMaxGroups groups of one grouped input x
 // [L, C]: one stats launch and one quantize launch (two with the rotation)
-// for all of them.  Groups with no rows are skipped.  ws: the groups'
-// control words and partials, laid out in group order (zero at rest).
+// for all of them.  Groups with no rows are skipped.  ctrl: the control
+// region (zero at rest); ws: the groups' partials, in group order.
 averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsigned flags, const GroupSpec* gs, int ng,
-                                     const GroupedGeom& geo, uint8_t* ws, DeviceInfo* dev, cudaStream_t s) {
+                                     const GroupedGeom& geo, unsigned* ctrl_region, uint8_t* ws, DeviceInfo* dev,
+                                     cudaStream_t s) {
   const bool split = (flags & AVERIS_MEAN_SPLIT) != 0;
   const bool had = (flags & AVERIS_HADAMARD16) != 0;
   GroupedStatsParams sp{};
@@ -423,8 +429,7 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
   for (int e = 0; e < ng; ++e) {
     const GroupSpec& G = gs[e];
     if (G.rows <= 0) continue;
-    unsigned* ctrl = reinterpret_cast<unsigned*>(ws);
-    ws += group_ctrl_bytes(geo);
+    unsigned* ctrl = ctrl_region + (size_t)n * kGroupCtrlWords;
     ColPartial* part = reinterpret_cast<ColPartial*>(ws);
     ws += group_part_bytes(geo, G.rows, C);
     const int nrb = (int)cdiv(G.rows, geo.rows_per);
@@ -562,12 +567,13 @@ averis_status grouped_quantize_impl(const void* x, int64_t L, int64_t C, unsigne
   averis_status st = device_info(&dev);
   if (st != AVERIS_OK) return st;
   const GroupedGeom geo = grouped_geom(L, C, std::min(ng, kMaxGroups));
-  uint8_t* w = static_cast<uint8_t*>(ws);
+  unsigned* ctrl = static_cast<unsigned*>(ws);  // reused by every chunk: each leaves it zero
+  uint8_t* w = static_cast<uint8_t*>(ws) + AVERIS_GROUPED_WORKSPACE_CTRL_BYTES;
   for (int e0 = 0; e0 < ng; e0 += kMaxGroups) {
     const int cnt = std::min(kMaxGroups, ng - e0);
-    if ((st = grouped_quantize_chunk(x, L, C, flags, gs + e0, cnt, geo, w, dev, s)) != AVERIS_OK) return st;
+    if ((st = grouped_quantize_chunk(x, L, C, flags, gs + e0, cnt, geo, ctrl, w, dev, s)) != AVERIS_OK) return st;
     for (int e = e0; e < e0 + cnt; ++e)
-      if (rows[e] > 0) w += group_ctrl_bytes(geo) + group_part_bytes(geo, rows[e], C);
+      if (rows[e] > 0) w += group_part_bytes(geo, rows[e], C);
   }
   return AVERIS_OK;
 }
