@@ -74,7 +74,7 @@ typedef enum {
 } averis_status;
 
 /* Size of the control block at the head of every workspace (zero at rest). */
-#define AVERIS_WORKSPACE_CTRL_BYTES 12544
+#define AVERIS_WORKSPACE_CTRL_BYTES 4352
 /* The same for the workspaces of the grouped (mixture-of-experts) calls. */
 #define AVERIS_GROUPED_WORKSPACE_CTRL_BYTES 278528
 

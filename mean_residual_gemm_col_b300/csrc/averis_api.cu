@@ -92,9 +92,9 @@ averis_status device_info(DeviceInfo** out) {
     cfg.blockDim = dim3(kGemmThreads);
     cfg.dynamicSmemBytes = GemmCfg<kSfbFull>::SMEM;
     int pairs = 0;
-    if (cudaOccupancyMaxActiveClusters(&pairs, gemm_nvfp4_kernel<true, kSfbFull, 1>, &cfg) != cudaSuccess || pairs < 1)
+    if (cudaOccupancyMaxActiveClusters(&pairs, gemm_nvfp4_kernel<kSfbFull, 1>, &cfg) != cudaSuccess || pairs < 1)
       return AVERIS_ERR_CUDA;
-    d.gemm_pairs = std::min(pairs, d.sms / 2);
+    d.gemm_pairs = std::min(std::min(pairs, d.sms / 2), kMaxPairs);
     d.attrs_set = true;
   }
   *out = &d;
@@ -125,17 +125,14 @@ averis_status set_attrs() {
   if (cudaFuncSetAttribute(split_quant_grouped_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kQSmem) != cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<false, kSfbFull, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<kSfbFull, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<true, kSfbFull, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<kSfbFull, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
     return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<false, kSfbFull, kMaxGemmGroups>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
-    return AVERIS_ERR_CUDA;
-  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<true, kSfbFull, kMaxGemmGroups>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
+  if (cudaFuncSetAttribute(gemm_nvfp4_kernel<kSfbFull, kMaxGemmGroups>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           GemmCfg<kSfbFull>::SMEM) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }
@@ -591,10 +588,12 @@ struct GemmSpec {
   float outer = 0.f;
   void* out = nullptr;
   int64_t ldo = 0;
+  bool bf16 = false;  // output in bf16 (else binary32)
 };
 
 // Argument checks of one GEMM (before anything touches the device).
-averis_status gemm_check(const GemmSpec& g, bool bf16) {
+averis_status gemm_check(const GemmSpec& g) {
+  const bool bf16 = g.bf16;
   const averis_nvfp4* a = g.a;
   const averis_nvfp4* b = g.b;
   if (a == nullptr || b == nullptr || g.out == nullptr) return AVERIS_ERR_INVALID_ARG;
@@ -610,8 +609,8 @@ averis_status gemm_check(const GemmSpec& g, bool bf16) {
 }
 
 // Fills one checked GEMM's tensor maps and scalars.
-averis_status gemm_fill(const GemmSpec& g, bool bf16, CUtensorMap* ta, CUtensorMap* tb, CUtensorMap* td,
-                        GemmGroup* gg) {
+averis_status gemm_fill(const GemmSpec& g, CUtensorMap* ta, CUtensorMap* tb, CUtensorMap* td, GemmGroup* gg) {
+  const bool bf16 = g.bf16;
   const averis_nvfp4* a = g.a;
   const averis_nvfp4* b = g.b;
   const int64_t M = a->rows, N = b->rows, K = a->cols;
@@ -641,55 +640,62 @@ averis_status gemm_fill(const GemmSpec& g, bool bf16, CUtensorMap* ta, CUtensorM
   gg->rb_a = (int)cdiv(M, 128);
   gg->rb_b = (int)cdiv(N, 128);
   gg->num_m = (int)cdiv(M, Cfg::PM);
+  gg->bf16 = bf16 ? 1 : 0;
   return AVERIS_OK;
 }
 
-// Up to G GEMMs (same output type) in one persistent launch of CTA pairs.
-// early_start: the kernel launched just before produced none of their inputs
-// (see GemmArgs::early_start).  splits > 1 (one binary32 GEMM only): split K
-// with partials in `part` and tickets in `tickets` (zero at rest).
+// Up to G GEMMs in one persistent launch of CTA pairs.  Each pair runs a
+// contiguous range of work units (GEMM after GEMM, tile after tile); the ranges
+// are cut so that every pair gets about the same cost, a unit costing its K
+// tiles plus an allowance for its epilogue, so that a launch mixing long-K
+// and short-K GEMMs (dW and dX of one layer, or the experts of a grouped
+// layer) keeps every pair busy.
 template <int G>
-averis_status gemm_launch(const GemmSpec* specs, int n, unsigned flags, cudaStream_t s, bool early_start,
-                          int splits = 1, float* part = nullptr, unsigned* tickets = nullptr) {
+averis_status gemm_launch(const GemmSpec* specs, int n, cudaStream_t s) {
   if (n < 1 || n > G) return AVERIS_ERR_INVALID_ARG;
-  const bool bf16 = (flags & AVERIS_OUT_BF16) != 0;
-  if (splits > 1 && (G != 1 || bf16 || part == nullptr || tickets == nullptr)) return AVERIS_ERR_INVALID_ARG;
   averis_status st = AVERIS_OK;
   for (int e = 0; e < n; ++e)
-    if ((st = gemm_check(specs[e], bf16)) != AVERIS_OK) return st;
+    if ((st = gemm_check(specs[e])) != AVERIS_OK) return st;
   DeviceInfo* dev = nullptr;
   if ((st = device_info(&dev)) != AVERIS_OK) return st;
   using Cfg = GemmCfg<kSfbFull>;
-  static thread_local GemmArgs<G> args;  // about 30 KB for G = 64: kept off the stack
+  static thread_local GemmArgs<G> args;  // about 31 KB for G = 64: kept off the stack
   std::memset(&args, 0, sizeof(args));
-  args.splits = splits > 1 ? splits : 1;
   int64_t units = 0;
+  double total = 0.0;
+  auto unit_cost = [](const GemmGroup& g) { return (double)(cdiv(g.kc, 4) + (g.bf16 ? 2 : 4)); };
   for (int e = 0; e < n; ++e) {
-    if ((st = gemm_fill(specs[e], bf16, &args.tmA[e], &args.tmB[e], &args.tmD[e], &args.g[e])) != AVERIS_OK)
-      return st;
+    if ((st = gemm_fill(specs[e], &args.tmA[e], &args.tmB[e], &args.tmD[e], &args.g[e])) != AVERIS_OK) return st;
     args.g[e].unit0 = (int)units;
-    units += (int64_t)args.g[e].num_m * cdiv(args.g[e].N, Cfg::BN) * args.splits;
+    const int64_t t = (int64_t)args.g[e].num_m * cdiv(args.g[e].N, Cfg::BN);
+    units += t;
+    total += (double)t * unit_cost(args.g[e]);
     if (units > (int64_t)1 << 30) return AVERIS_ERR_INVALID_ARG;
   }
   args.ngroups = n;
   args.nunits = (int)units;
   args.err = dev->err_word;
   args.wait_limit = kWaitLimit;
-  args.early_start = early_start ? 1 : 0;
-  args.part = part;
-  args.tickets = tickets;
-  // pairs of CTAs (clusters of two), at most the pairs resident at once
-  const int grid = 2 * (int)std::min<int64_t>(units, dev->gemm_pairs);
-  cudaError_t e = bf16 ? launch_pdl(gemm_nvfp4_kernel<true, kSfbFull, G>, dim3(grid), dim3(kGemmThreads), Cfg::SMEM,
-                                    s, args)
-                       : launch_pdl(gemm_nvfp4_kernel<false, kSfbFull, G>, dim3(grid), dim3(kGemmThreads),
-                                    Cfg::SMEM, s, args);
-  return e == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA;
+  args.early_start = 0;
+  const int pairs = (int)std::min<int64_t>(units, dev->gemm_pairs);
+  // contiguous cost-balanced ranges: pair p ends at the first unit whose cost
+  // prefix reaches (p + 1) / pairs of the total
+  int p = 0, e = 0;
+  double acc = 0.0;
+  args.range0[0] = 0;
+  for (int64_t u = 0; u < units && p < pairs - 1; ++u) {
+    while (e + 1 < n && args.g[e + 1].unit0 <= u) ++e;
+    acc += unit_cost(args.g[e]);
+    if (acc >= total * (double)(p + 1) / (double)pairs) args.range0[++p] = (int)(u + 1);
+  }
+  while (p < pairs) args.range0[++p] = (int)units;
+  const cudaError_t err =
+      launch_pdl(gemm_nvfp4_kernel<kSfbFull, G>, dim3(2 * pairs), dim3(kGemmThreads), Cfg::SMEM, s, args);
+  return err == cudaSuccess ? AVERIS_OK : AVERIS_ERR_CUDA;
 }
 
 averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const float* col_add, const float* row_vec,
-                        const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s,
-                        bool early_start = false, int splits = 1, float* part = nullptr, unsigned* tickets = nullptr) {
+                        const float* col_vec, float outer, void* out, int64_t ldo, unsigned flags, cudaStream_t s) {
   GemmSpec g;
   g.a = a;
   g.b = b;
@@ -699,14 +705,14 @@ averis_status gemm_impl(const averis_nvfp4* a, const averis_nvfp4* b, const floa
   g.outer = outer;
   g.out = out;
   g.ldo = ldo;
-  return gemm_launch<1>(&g, 1, flags, s, early_start, splits, part, tickets);
+  g.bf16 = (flags & AVERIS_OUT_BF16) != 0;
+  return gemm_launch<1>(&g, 1, s);
 }
 
-// Many GEMMs (same output type), kMaxGemmGroups per launch.
-averis_status grouped_gemm_impl(const GemmSpec* specs, int n, unsigned flags, cudaStream_t s, bool early_start) {
+// Many GEMMs, kMaxGemmGroups per launch.
+averis_status grouped_gemm_impl(const GemmSpec* specs, int n, cudaStream_t s) {
   for (int e0 = 0; e0 < n; e0 += kMaxGemmGroups) {
-    const int cnt = std::min(kMaxGemmGroups, n - e0);
-    const averis_status st = gemm_launch<kMaxGemmGroups>(specs + e0, cnt, flags, s, early_start && e0 == 0);
+    const averis_status st = gemm_launch<kMaxGemmGroups>(specs + e0, std::min(kMaxGemmGroups, n - e0), s);
     if (st != AVERIS_OK) return st;
   }
   return AVERIS_OK;
@@ -757,38 +763,9 @@ averis_nvfp4 carve_nvfp4(Carver& c, int64_t rows, int64_t cols) {
 
 size_t fwd_ws(int64_t l, int64_t m, int64_t n) { return quant_ws_bytes(l, m) + align256((size_t)n * 4); }
 
-// Split K of the weight-gradient GEMM (M = m, N = n, K = l): how many K
-// ranges each 256 x 256 tile is cut into.  Chosen from the shape alone (with
-// the pair count of a 148-SM B300), so that the workspace size does not
-// depend on the device: the fewest ranges whose modelled time -- waves of
-// units times (K tiles per range + epilogue, + partial traffic when split)
-// -- is clearly the shortest, with at least four K tiles per range.
-constexpr int64_t kNominalPairs = 74;
-int dw_splits(int64_t M, int64_t N, int64_t K) {
-  const int64_t tiles = cdiv(M, 256) * cdiv(N, 256);
-  const int64_t nkt = cdiv(cdiv(K, 64), 4);
-  if (tiles * 2 > kMaxGemmTickets) return 1;  // its tickets live in the workspace's control block
-  int best = 1;
-  double best_t = 0.0;
-  for (int S = 1; S <= 4; ++S) {
-    if (S > 1 && nkt < 4 * S) break;
-    const double t = (double)cdiv(tiles * S, kNominalPairs) * ((double)cdiv(nkt, S) + 2.0 + (S > 1 ? 2.0 : 0.0));
-    if (S == 1 || t < 0.9 * best_t) {
-      best = S;
-      best_t = t;
-    }
-  }
-  return best;
-}
-size_t dw_split_part_bytes(int64_t M, int64_t N, int64_t K) {
-  const int S = dw_splits(M, N, K);
-  if (S == 1) return 0;
-  return align256((size_t)cdiv(M, 256) * cdiv(N, 256) * S * 2 * 256 * 128 * sizeof(float));
-}
-
 size_t bwd_ws(int64_t l, int64_t m, int64_t n) {
   return quant_ws_bytes(l, n) + nvfp4_bytes(l, n) + nvfp4_bytes(n, l) + nvfp4_bytes(1, n) +
-         2 * align256((size_t)n * 4) + align256((size_t)m * 4) + dw_split_part_bytes(m, n, l);
+         2 * align256((size_t)n * 4) + align256((size_t)m * 4);
 }
 
 averis_status linear_fwd_impl(const void* x, int64_t l, int64_t m, int64_t n, const averis_nvfp4* w_m, unsigned flags,
@@ -826,19 +803,25 @@ averis_status linear_bwd_impl(const void* d, int64_t l, int64_t m, int64_t n, co
   float* mu = static_cast<float*>(c.take((size_t)n * 4));
   float* mu_hat = static_cast<float*>(c.take((size_t)n * 4));
   float* r_d = static_cast<float*>(c.take((size_t)m * 4));
-  const int splits = dw_splits(m, n, l);
-  // the tickets sit in the control block at the workspace's head (zero at rest for every shape)
-  unsigned* tickets = splits > 1 ? static_cast<unsigned*>(qws) + kCtrlGemmTicket : nullptr;
-  float* part = splits > 1 ? static_cast<float*>(c.take(dw_split_part_bytes(m, n, l))) : nullptr;
   averis_status r = quantize_impl(d, l, n, flags, mu, &mu_q, mu_hat, &d_row, &d_col, qws, quant_ws_bytes(l, n), s,
                                   split ? w_n : nullptr, split ? r_d : nullptr);
   if (r != AVERIS_OK) return r;
-  if ((r = gemm_impl(&d_row, w_n, split ? r_d : nullptr, nullptr, nullptr, 0.f, dx, m, flags, s)) != AVERIS_OK)
-    return r;
-  // dW reads the forward state and D's quantized column layout, not dX: it
-  // starts while the input-gradient GEMM drains
-  return gemm_impl(&st->x_col, &d_col, nullptr, split ? st->mu_hat : nullptr, split ? mu_hat : nullptr, (float)l, dw,
-                   n, flags & ~AVERIS_OUT_BF16, s, /*early_start=*/true, splits, part, tickets);
+  // dW (long K: the tokens) and dX in one launch, the pairs' ranges balanced by cost
+  GemmSpec g[2];
+  g[0].a = &st->x_col;
+  g[0].b = &d_col;
+  g[0].row_vec = split ? st->mu_hat : nullptr;
+  g[0].col_vec = split ? mu_hat : nullptr;
+  g[0].outer = (float)l;
+  g[0].out = dw;
+  g[0].ldo = n;
+  g[1].a = &d_row;
+  g[1].b = w_n;
+  g[1].col_add = split ? r_d : nullptr;
+  g[1].out = dx;
+  g[1].ldo = m;
+  g[1].bf16 = (flags & AVERIS_OUT_BF16) != 0;
+  return gemm_launch<2>(g, 2, s);
 }
 
 // Zeroes the control block of the allocation-free call's scratch on this
@@ -1030,9 +1013,10 @@ averis_status averis_grouped_linear_fwd(const void* x, const int64_t* offsets, i
     g.col_add = split ? r_x[(size_t)e] : nullptr;
     g.out = static_cast<uint8_t*>(y) + offsets[e] * n * esz;
     g.ldo = n;
+    g.bf16 = esz == 2;
     gm.push_back(g);
   }
-  return grouped_gemm_impl(gm.data(), (int)gm.size(), flags, stream, false);
+  return grouped_gemm_impl(gm.data(), (int)gm.size(), stream);
 }
 
 averis_status averis_grouped_linear_bwd(const void* d, const int64_t* offsets, int64_t num_experts, int64_t m,
@@ -1102,6 +1086,7 @@ averis_status averis_grouped_linear_bwd(const void* d, const int64_t* offsets, i
     a.col_add = split ? D.r_d : nullptr;
     a.out = static_cast<uint8_t*>(dx) + offsets[e] * m * esz;
     a.ldo = m;
+    a.bf16 = esz == 2;
     gx.push_back(a);
     GemmSpec w;
     w.a = &states[e].x_col;
@@ -1113,9 +1098,9 @@ averis_status averis_grouped_linear_bwd(const void* d, const int64_t* offsets, i
     w.ldo = n;
     gw.push_back(w);
   }
-  if ((r = grouped_gemm_impl(gx.data(), (int)gx.size(), flags, stream, false)) != AVERIS_OK) return r;
-  // the weight gradients read the forward states and D's column layouts, not dX
-  return grouped_gemm_impl(gw.data(), (int)gw.size(), flags & ~AVERIS_OUT_BF16, stream, true);
+  // the weight gradients first (the longest units), then the input gradients
+  if ((r = grouped_gemm_impl(gw.data(), (int)gw.size(), stream)) != AVERIS_OK) return r;
+  return grouped_gemm_impl(gx.data(), (int)gx.size(), stream);
 }
 
 const char* averis_status_string(averis_status status) {

@@ -17,8 +17,11 @@
 // CTA loads its own 128 rows of A and its own 128 rows of B (half of the
 // tile's N), so every SM streams 32 KB of operands per 256-element K tile
 // instead of the 48 KB a one-CTA 128 x 256 tile needs, and the shared-memory
-// ring is deeper for the same capacity.  Tiles run M fastest, so pairs
-// running together share B tiles in L2.  Warp roles, in each CTA:
+// ring is deeper for the same capacity.  A launch runs up to G GEMMs (the
+// dW and dX of a layer, or the experts of a grouped layer), each with its own
+// output type; every pair runs a contiguous range of work units (GEMM after
+// GEMM, tiles M fastest), the ranges cut by the host so that the pairs' K
+// tiles balance.  Warp roles, in each CTA:
 //   warp 0     TMA producer: this CTA's A and B halves by 2-D tensor TMA
 //              (128-byte swizzle), completing on the leader CTA's stage
 //              barrier; block scales by 1-D bulk copies into its own SMEM.
@@ -64,7 +67,10 @@ struct GemmGroup {
   int rb_b;    // ceil(N / 128): row chunks of B's scales
   int num_m;   // ceil(M / 256): pair tiles along M
   int unit0;   // first work unit of this GEMM in the launch
+  int bf16;    // output in bf16 (else binary32)
 };
+
+constexpr int kMaxPairs = 128;  // CTA pairs of one launch at most (74 on a B300)
 
 // Kernel arguments for up to G GEMMs: their tensor maps (A, B codes and the
 // output, kept in parameter space, where TMA reads them) and scalars.
@@ -76,19 +82,15 @@ struct GemmArgs {
   int nunits;          // work units of all GEMMs
   int* err;
   long long wait_limit;  // bound of every wait, in SM clock cycles
-  // 1: none of this GEMM's inputs comes from the kernel launched just before
-  // it (the library issues it right after an independent GEMM): start at
-  // once, and wait for that kernel only before exiting, so that this
-  // kernel's completion still implies the previous one's.
+  // 1: none of these GEMMs' inputs comes from the kernel launched just before
+  // (the library never sets it today): start at once, and wait for that kernel
+  // only before exiting, so that this kernel's completion still implies the
+  // previous one's.
   int early_start;
-  // split K (one GEMM, binary32 output only): every tile's K tiles are cut
-  // into `splits` contiguous ranges computed by different pairs; each writes
-  // its raw accumulator to `part`, and the last of a tile's ranges to finish
-  // (ticket in `tickets`, zero at rest) adds them up in range order and runs
-  // the epilogue.  splits == 1: no partials.
-  int splits;
-  float* part;        // [tiles * splits][2 CTAs][BN columns][128 rows]
-  unsigned* tickets;  // [tiles][2 CTAs]
+  // pair p runs the contiguous units range0[p] .. range0[p+1]-1, cut by the
+  // host so that every pair gets about the same number of K tiles (units of
+  // different GEMMs of a launch can differ widely in K)
+  int range0[kMaxPairs + 1];
 };
 // kernel parameters are limited to 32764 bytes
 constexpr int kMaxGemmGroups = 64;
@@ -149,7 +151,7 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // warps: producer, TMEM owner / MMA issuer, 8 epilogue warps, 4 scale-feed warps
 constexpr int kGemmThreads = 32 * (2 + 8 + 4);
 
-template <bool BF16_OUT, bool SFB_FULL, int G>
+template <bool SFB_FULL, int G>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     gemm_nvfp4_kernel(const __grid_constant__ GemmArgs<G> p) {
   using Cfg = GemmCfg<SFB_FULL>;
@@ -201,11 +203,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   else
     ptx::pdl_wait_and_release();
 
-  const int nunits = p.nunits;
-  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int pair = blockIdx.x >> 1;
+  const int u_begin = p.range0[pair], u_end = p.range0[pair + 1];
   // work unit -> its GEMM (the last one whose first unit is not after it),
-  // output tile (mt, nt), M fastest, and K-tile range; the ranges of one tile
-  // are consecutive units, so they run at the same time
+  // output tile (mt, nt), M fastest, and K-tile range (all of K)
   struct Unit {
     int e, tile, mt, nt, kt0, kt1;
   };
@@ -222,14 +223,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       u.e = lo;
     }
     const GemmGroup& gg = p.g[u.e];
-    const int local = unit - gg.unit0;
-    u.tile = local / p.splits;
-    const int sp = local - u.tile * p.splits;
+    u.tile = unit - gg.unit0;
     u.mt = u.tile % gg.num_m;
     u.nt = u.tile / gg.num_m;
-    const int nkt = (gg.kc + 3) / 4;
-    u.kt0 = (int)(((long long)sp * nkt) / p.splits);
-    u.kt1 = (int)(((long long)(sp + 1) * nkt) / p.splits);
+    u.kt0 = 0;
+    u.kt1 = (gg.kc + 3) / 4;
     return u;
   };
 
@@ -240,7 +238,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t issued = 0;  // stages this thread has filled at least once (bit mask)
       bool failed = false;
       int cur_e = -1;
-      for (int unit = pair; unit < nunits && !failed; unit += npairs) {
+      for (int unit = u_begin; unit < u_end && !failed; ++unit) {
         const Unit u = decode(unit);
         const GemmGroup& gg = p.g[u.e];
         const CUtensorMap* tmA = &p.tmA[u.e];
@@ -308,7 +306,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       bool issued = false;
-      for (int unit = pair; unit < nunits; unit += npairs, ++it) {
+      for (int unit = u_begin; unit < u_end; ++unit, ++it) {
         const Unit u = decode(unit);
         const int kc = p.g[u.e].kc, kt0 = u.kt0, kt1 = u.kt1;
         if (!ptx::mbar_wait(tempty, (it & 1) ^ 1u, p.wait_limit)) {
@@ -362,7 +360,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool failed = false;
-    for (int unit = pair; unit < nunits && !failed; unit += npairs) {
+    for (int unit = u_begin; unit < u_end && !failed; ++unit) {
       const Unit u = decode(unit);
       for (int kt = u.kt0; kt < u.kt1; ++kt) {
         if (!ptx::mbar_wait(&sf_loaded[stage], phase, p.wait_limit)) {
@@ -421,10 +419,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     float* vec_base = reinterpret_cast<float*>(smem + Cfg::OFF_VEC);
     const uint32_t tempty_leader = ptx::mapa(ptx::smem_u32(tempty), 0);
     __shared__ int s_ok[2];    // per tile parity: the accumulator arrived
-    __shared__ int s_last[2];  // per tile parity: this unit adds up the tile's partials
     int it = 0;
     int cur_e = -1;
-    for (int unit = pair; unit < nunits; unit += npairs, ++it) {
+    for (int unit = u_begin; unit < u_end; ++unit, ++it) {
       const Unit u = decode(unit);
       const GemmGroup& gg = p.g[u.e];
       const CUtensorMap* tmD = &p.tmD[u.e];
@@ -480,7 +477,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         if (lane == 0) ptx::mbar_arrive_cluster(tempty_leader);
       };
 
-      if constexpr (BF16_OUT) {
+      if (gg.bf16) {
         // this warp's accumulator columns -> packed bf16 registers, release TMEM, then store
         uint32_t packed[Cfg::EPI_COLS / 2];
 #pragma unroll
@@ -521,52 +518,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           }
         }
       } else {
-        bool reduce = false;  // this unit is the last of its tile's K ranges: add up the partials
-        if (p.splits > 1) {
-          // raw accumulator -> this unit's partial, [column][row] so that a warp's
-          // 32 rows of one column are 128 contiguous bytes
-          float* mine = p.part + ((size_t)unit * 2 + cta) * (size_t)(BN * Cfg::BM) + q * 32 + lane;
-#pragma unroll 1
-          for (int c = cb; c < cb + Cfg::EPI_COLS; c += 32) {
-            uint32_t v[32];
-            ptx::tmem_ld32(t_row + (uint32_t)c, v);
-            ptx::tmem_ld_wait();
-            if (c + 32 == cb + Cfg::EPI_COLS) release();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) __stcg(mine + (size_t)(c + j) * Cfg::BM, __uint_as_float(v[j]));
-          }
-          __threadfence();
-          epi_bar<EPI_WARPS>();
-          if (et == 0) {
-            unsigned* tk = p.tickets + (size_t)u.tile * 2 + cta;
-            const unsigned t = atomicAdd(tk, 1u);
-            s_last[it & 1] = (t == (unsigned)p.splits - 1) ? 1 : 0;
-            if (t == (unsigned)p.splits - 1) *tk = 0u;  // every range has arrived: zero at rest again
-          }
-          epi_bar<EPI_WARPS>();
-          reduce = s_last[it & 1] != 0;
-          if (!reduce) continue;
-          __threadfence();
-        }
 #pragma unroll 1
         for (int c = cb; c < cb + Cfg::EPI_COLS; c += 32) {
           uint32_t v[32];
-          if (reduce) {
-            // sum of the tile's partials in range order (the same bits whichever range is last)
-            const float* base = p.part + (size_t)u.tile * p.splits * 2 * (size_t)(BN * Cfg::BM) +
-                                (size_t)cta * (BN * Cfg::BM) + (size_t)c * Cfg::BM + q * 32 + lane;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__ldcg(base + (size_t)j * Cfg::BM));
-            for (int sp = 1; sp < p.splits; ++sp) {
-              const float* b2 = base + (size_t)sp * 2 * (BN * Cfg::BM);
-#pragma unroll
-              for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(b2 + (size_t)j * Cfg::BM));
-            }
-          } else {
-            ptx::tmem_ld32(t_row + (uint32_t)c, v);
-            ptx::tmem_ld_wait();
-            if (c + 32 == cb + Cfg::EPI_COLS) release();  // last chunk is in registers
-          }
+          ptx::tmem_ld32(t_row + (uint32_t)c, v);
+          ptx::tmem_ld_wait();
+          if (c + 32 == cb + Cfg::EPI_COLS) release();  // last chunk is in registers
           if (!rows_live) continue;
           const float* ca = cadd_s + c;
           const float* cv = cvec_s + c;

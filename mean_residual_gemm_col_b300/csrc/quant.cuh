@@ -41,9 +41,7 @@ enum : int {
   kCtrlQuantTicket = 7,  // quantize pass: CTAs finished
   kCtrlStrip = 64,       // per-strip-group tickets of the stats pass
   kMaxStripGroups = 1024,
-  kCtrlGemmTicket = kCtrlStrip + kMaxStripGroups,  // split-K tickets of a GEMM sharing the workspace
-  kMaxGemmTickets = 2048,
-  kCtrlWords = kCtrlGemmTicket + kMaxGemmTickets
+  kCtrlWords = kCtrlStrip + kMaxStripGroups
 };
 
 struct ColPartial {
