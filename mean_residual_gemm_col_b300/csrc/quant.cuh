@@ -263,14 +263,22 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
   __shared__ float red[8];
   __shared__ int s_last;
   __shared__ uint64_t s_full[kStatsBufs];
-  __shared__ int s_ok;
+  __shared__ int s_done[kStatsBufs];  // warps done with the buffer's current box
+  __shared__ int s_failed;
+  __shared__ int s_issued;  // boxes of the current strip requested so far
   if (threadIdx.x == 0) {
-    for (int b = 0; b < kStatsBufs; ++b) ptx::mbar_init(&s_full[b], 1);
+    for (int b = 0; b < kStatsBufs; ++b) {
+      ptx::mbar_init(&s_full[b], 1);
+      s_done[b] = 0;
+    }
+    s_failed = 0;
     ptx::fence_mbar_init();
     ptx::prefetch_tmap(&tmX);
   }
   __syncthreads();
   ptx::pdl_wait_and_release();
+  // the quantize pass reads X again right after: keep its lines in L2
+  const uint64_t keep = ptx::l2_policy_evict_last();
   uint32_t it = 0;  // boxes consumed by this CTA (buffer it % kStatsBufs, phase it / kStatsBufs)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -321,29 +329,34 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
     // rl, rl + 32, ... of a box are one 8-row group.  Rows past this CTA's block
     // are left out (max / min see a repeat of a counted row, the sum zeros).
     const int64_t nbox = (rb1 - rb0 + kStatsBoxRows - 1) / kStatsBoxRows;
-    if (threadIdx.x == 0 && !p.starve)
-      for (int64_t k = 0; k < kStatsBufs && k < nbox; ++k) {
-        const uint32_t b = (it + (uint32_t)k) % kStatsBufs;
-        ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
-        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64, (int32_t)(p.row_base + rb0 + k * kStatsBoxRows),
-                         &s_full[b]);
-      }
+    if (threadIdx.x == 0) {
+      s_issued = 0;
+      if (!p.starve)
+        for (int64_t k = 0; k < kStatsBufs && k < nbox; ++k) {
+          const uint32_t b = (it + (uint32_t)k) % kStatsBufs;
+          ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
+          ptx::tma_load_2d_hint(ring + b * kStatsBox, &tmX, strip * 64,
+                                (int32_t)(p.row_base + rb0 + k * kStatsBoxRows), &s_full[b], keep);
+          s_issued = (int)k + 1;
+        }
+    }
+    __syncthreads();
+    // every warp walks the boxes on its own; the last warp done with a box
+    // refills its buffer (no CTA-wide barrier per box)
+    uint32_t it0 = it;  // first box of this strip
     for (int64_t k = 0; k < nbox; ++k, ++it) {
       const uint32_t b = it % kStatsBufs;
-      if (threadIdx.x == 0) s_ok = ptx::mbar_wait(&s_full[b], (it / kStatsBufs) & 1u, p.wait_limit) ? 1 : 0;
-      __syncthreads();
-      if (!s_ok) {
-        // every thread gives up together: report, let the boxes still in flight
-        // land (bounded), and still take the ticket below so that the control
-        // block returns to zero; the results of this call are invalid
-        if (threadIdx.x == 0) {
+      int ok = 1;
+      if (lane == 0) ok = ptx::mbar_wait(&s_full[b], (it / kStatsBufs) & 1u, p.wait_limit) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) {
+        // this warp gives up; the others give up on their own waits.  The
+        // results of this call are invalid; the CTA still takes its ticket
+        // below so that the control block returns to zero
+        if (lane == 0) {
           atomicExch(p.err, kErrQuantLoad);
-          const int64_t issued = p.starve ? k : min(nbox, k + (int64_t)kStatsBufs);
-          for (int64_t j = k + 1; j < issued; ++j)
-            ptx::mbar_wait(&s_full[(it + (uint32_t)(j - k)) % kStatsBufs],
-                           ((it + (uint32_t)(j - k)) / kStatsBufs) & 1u, p.wait_limit);
+          s_failed = 1;
         }
-        failed = true;
         break;
       }
       const int64_t row0 = rb0 + k * kStatsBoxRows + rl;  // this thread's first row of the box
@@ -365,14 +378,35 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
         else
           group(v, nv);
       }
-      __syncthreads();  // the buffer is free
-      if (threadIdx.x == 0 && k + kStatsBufs < nbox) {
-        ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
-        ptx::tma_load_2d(ring + b * kStatsBox, &tmX, strip * 64,
-                         (int32_t)(p.row_base + rb0 + (k + kStatsBufs) * kStatsBoxRows), &s_full[b]);
+      // count this warp done with the box; the last of the 8 warps refills the buffer
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence_block();
+        if (atomicAdd(&s_done[b], 1) == 7) {
+          s_done[b] = 0;
+          if (k + kStatsBufs < nbox) {
+            ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
+            ptx::tma_load_2d_hint(ring + b * kStatsBox, &tmX, strip * 64,
+                                  (int32_t)(p.row_base + rb0 + (k + kStatsBufs) * kStatsBoxRows), &s_full[b], keep);
+            s_issued = (int)(k + kStatsBufs) + 1;
+          }
+        }
       }
     }
-    if (failed) break;
+    __syncthreads();  // every warp is done with this strip's boxes (or gave up)
+    if (s_failed) {
+      if (threadIdx.x == 0) {
+        // let the boxes still in flight land (bounded) before the buffers are
+        // given up: only the last kStatsBufs requested can be (a box is
+        // requested only after the box kStatsBufs before it was consumed)
+        for (int k = max(0, s_issued - kStatsBufs); k < s_issued; ++k)
+          ptx::mbar_wait(&s_full[(it0 + (uint32_t)k) % kStatsBufs], ((it0 + (uint32_t)k) / kStatsBufs) & 1u,
+                         p.wait_limit);
+      }
+      failed = true;
+      break;
+    }
+    it = it0 + (uint32_t)nbox;
     // combine the 4 row lanes of this warp that share the columns (lanes differ by 8, 16)
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
@@ -890,8 +924,10 @@ __device__ __forceinline__ void split_quant_body(const CUtensorMap& tmX, const Q
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     ptx::mbar_arrive_expect_tx(&full[b], (uint32_t)kQTileBytes + (split ? mu_bytes(tile) : 0u));
     const int32_t y = (int32_t)(p.row_base + (int64_t)tr * kQTile);
-    ptx::tma_load_2d(sm + b * kQTileBytes, &tmX, tc * kQTile, y, &full[b]);
-    ptx::tma_load_2d(sm + b * kQTileBytes + kQHalf, &tmX, tc * kQTile + 64, y, &full[b]);
+    // the last read of X in this call (the stats pass kept it in L2)
+    const uint64_t last_use = ptx::l2_policy_evict_first();
+    ptx::tma_load_2d_hint(sm + b * kQTileBytes, &tmX, tc * kQTile, y, &full[b], last_use);
+    ptx::tma_load_2d_hint(sm + b * kQTileBytes + kQHalf, &tmX, tc * kQTile + 64, y, &full[b], last_use);
   };
   auto issue_mu = [&](int tile, int b) {
     if (split) ptx::bulk_load(mu_s + 128 * b, p.mu + (int64_t)(tile % p.tiles_c) * kQTile, mu_bytes(tile), &full[b]);
