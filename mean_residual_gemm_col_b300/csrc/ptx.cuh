@@ -290,6 +290,15 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading
 // and stride byte offsets, fixed version bits 46..48 = 0b001, layout type.
+// One 32-row x 16-byte shared-memory matrix (descriptor `sdesc`) copied into
+// 4 TMEM columns at `taddr` of every lane quarter (row i -> lanes i, 32 + i,
+// 64 + i, 96 + i): the block-scale layout of the MMA.  Issued by one thread
+// for the pair: each CTA's own shared memory into its own TMEM, executed in
+// issue order with the thread's MMAs.
+__device__ __forceinline__ void tc_cp_scales_pair(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 enum : uint32_t { kSwizzleNone = 0, kSwizzle128B = 2 };
 __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
                                               uint32_t layout) {
