@@ -48,7 +48,7 @@ CPU_SAMPLE_TOKENS = 256
 # launches that the per-kernel timing replays (NVTX range gemm_group_timed) in
 # one ncu capture, keyed by a hash of the GEMM source the capture was taken
 # on; any other source reports null.
-GEMM_TRAFFIC = {"c8581fbd97ab5c73": 250.9e6 / 12}
+GEMM_TRAFFIC = {"ce8abe9ccb8c30a6": 244.93e6 / 12}
 
 
 def gemm_traffic_per_launch():
