@@ -48,7 +48,7 @@ CPU_SAMPLE_TOKENS = 256
 # launches that the per-kernel timing replays (NVTX range gemm_group_timed) in
 # one ncu capture, keyed by a hash of the GEMM source the capture was taken
 # on; any other source reports null.
-GEMM_TRAFFIC = {"ce8abe9ccb8c30a6": 244.93e6 / 12}
+GEMM_TRAFFIC = {"e51e38f75f972bb7": 244.87e6 / 12}
 
 
 def gemm_traffic_per_launch():
@@ -841,17 +841,39 @@ def stack_comparison(steps=3, warmup=2):
 # --------------------------------------------------------- CPU baseline ----
 
 def blas_threads():
-    """Threads of the BLAS NumPy calls into (threadpoolctl), else the OpenMP setting."""
+    """Threads of the BLAS NumPy calls into (threadpoolctl), else the OpenMP
+    setting; with a note saying where the number came from (or why not)."""
+    note = "threadpoolctl"
     try:
         from threadpoolctl import threadpool_info
 
-        n = [p["num_threads"] for p in threadpool_info() if p.get("user_api") == "blas"]
+        info = threadpool_info()
+        n = [p["num_threads"] for p in info if p.get("user_api") == "blas"]
         if n:
-            return max(n)
-    except Exception:
-        pass
+            return max(n), "threadpoolctl: " + ", ".join(sorted({str(p.get("internal_api")) for p in info
+                                                                  if p.get("user_api") == "blas"}))
+        note = "threadpoolctl found no BLAS among " + ", ".join(str(p.get("internal_api")) for p in info)
+    except Exception as e:  # report, do not fail the bench
+        note = f"threadpoolctl unavailable: {type(e).__name__}"
+    # the OpenBLAS that NumPy loaded, asked directly (its exported thread-count query)
+    try:
+        import ctypes
+
+        with open("/proc/self/maps") as fh:
+            libs = sorted({ln.split()[-1] for ln in fh if "openblas" in ln.lower() and ln.rstrip().endswith(".so")})
+        for lib in libs:
+            so = ctypes.CDLL(lib)
+            for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_", "openblas_get_num_threads"):
+                fn = getattr(so, sym, None)
+                if fn is not None:
+                    fn.restype = ctypes.c_int
+                    return int(fn()), note + f"; {os.path.basename(lib)} {sym}()"
+    except Exception as e:
+        note += f"; OpenBLAS query failed: {type(e).__name__}"
     v = os.environ.get("OMP_NUM_THREADS")
-    return int(v) if v and v.isdigit() else None
+    if v and v.isdigit():
+        return int(v), note + "; OMP_NUM_THREADS"
+    return None, note
 
 
 def cpu_baseline(target_s=10.0):
@@ -878,9 +900,10 @@ def cpu_baseline(target_s=10.0):
         rep += 1
         if t_total >= target_s:
             break
-    threads = blas_threads()                # after the oracle ran: its BLAS is loaded by now
+    threads, note = blas_threads()          # after the oracle ran: its BLAS is loaded by now
     return {"value": round(total_flops / t_total / 1e12, 6), "unit": "TFLOP/s",
             "cores": threads or os.cpu_count(), "host_cpus": os.cpu_count(), "blas_threads": threads,
+            "blas_threads_source": note,
             "kind": "oracle",
             "sample": f"{rep} x ({tok} of {L} tokens of each of the 4 linears, fwd+bwd), float64 NumPy, "
                       f"{t_total:.1f} s"}

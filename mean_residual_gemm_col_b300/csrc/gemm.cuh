@@ -329,11 +329,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           const uint32_t sfb_t = sfa_t + 16u;
           const uint32_t a_s = ptx::smem_u32(smem + Cfg::OFF_A + stage * Cfg::A_BYTES);
           const uint32_t b_s = ptx::smem_u32(smem + Cfg::OFF_B + stage * Cfg::B_BYTES);
-          for (int g = 0; g < ns; ++g) {
-            const uint64_t adesc = ptx::smem_desc(a_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
-            const uint64_t bdesc = ptx::smem_desc(b_s + 32u * g, 16u, 1024u, ptx::kSwizzle128B);
-            ptx::tc_mma_nvf4_pair(tmem, adesc, bdesc, Cfg::IDESC, sfa_t + 4u * g,
-                                  sfb_t + (uint32_t)(Cfg::SFB_STEP * g), (kt != kt0 || g != 0) ? 1u : 0u);
+          const uint64_t adesc0 = ptx::smem_desc(a_s, 16u, 1024u, ptx::kSwizzle128B);
+          const uint64_t bdesc0 = ptx::smem_desc(b_s, 16u, 1024u, ptx::kSwizzle128B);
+          const uint32_t acc0 = kt != kt0 ? 1u : 0u;
+          if (ns == 4) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g)
+              ptx::tc_mma_nvf4_pair(tmem, adesc0 + 2u * g, bdesc0 + 2u * g, Cfg::IDESC, sfa_t + 4u * g,
+                                    sfb_t + (uint32_t)(Cfg::SFB_STEP * g), g != 0 ? 1u : acc0);
+          } else {
+            for (int g = 0; g < ns; ++g)
+              ptx::tc_mma_nvf4_pair(tmem, adesc0 + 2u * g, bdesc0 + 2u * g, Cfg::IDESC, sfa_t + 4u * g,
+                                    sfb_t + (uint32_t)(Cfg::SFB_STEP * g), g != 0 ? 1u : acc0);
           }
           issued = true;
           ptx::tc_commit_pair(&empty[stage], 0x3);
