@@ -36,7 +36,8 @@
 //   warps 10-13 scale feed: write each stage's block scales from SMEM into
 //              this CTA's TMEM with tcgen05.st (the words a 32x128b.warpx4
 //              copy of each scale atom would place), then arrive on the
-//              leader's barrier, so the MMA thread issues only MMAs.
+//              leader's stage barrier, the one the operands complete on, so
+//              the MMA thread waits once per stage and issues only MMAs.
 // Every wait is bounded; on timeout the kernel sets the error word, lets its
 // copies in flight land, drains its tensor-core work, and both CTAs meet at a
 // cluster barrier before freeing TMEM.  Launched with programmatic dependent
@@ -160,11 +161,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   constexpr int EPI_WARPS = Cfg::EPI_WARPS;
   extern __shared__ uint8_t gsm_raw[];
   uint8_t* smem = gsm_raw + ((1024u - (ptx::smem_u32(gsm_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);  // [STAGES] leader: both CTAs' operands landed
+  // [STAGES] leader: both CTAs' operands landed and both CTAs' scales are in TMEM
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
   uint64_t* empty = full + STAGES;       // [STAGES] both: the stage's MMAs completed
   uint64_t* sf_loaded = empty + STAGES;  // [STAGES] both: this CTA's scale atoms are in SMEM
-  uint64_t* sf_full = sf_loaded + STAGES;  // [STAGES] leader: both CTAs' scales are in TMEM
-  uint64_t* tfull = sf_full + STAGES;    // both: the accumulator holds a finished tile
+  uint64_t* tfull = sf_loaded + STAGES;  // both: the accumulator holds a finished tile
   uint64_t* tempty = tfull + 1;          // leader: both CTAs' epilogues drained the accumulator
   uint64_t* drain = tempty + 1;          // leader: every MMA issued has completed
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -173,10 +174,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
   const uint32_t cta = ptx::cluster_ctarank();  // 0: leader (issues the MMAs), 1: follower
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&full[s], 1 + 2 * 4);  // the leader's producer (with the bytes), the scale warps of both CTAs
       ptx::mbar_init(&empty[s], 1);
       ptx::mbar_init(&sf_loaded[s], 1);
-      ptx::mbar_init(&sf_full[s], 2 * 4);
     }
     ptx::mbar_init(tfull, 1);
     ptx::mbar_init(tempty, 2 * EPI_WARPS);
@@ -316,9 +316,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         ptx::tc_fence_after();
         bool ok = true;
         for (int kt = kt0; kt < kt1; ++kt) {
-          // both CTAs' operand tiles in SMEM, both CTAs' scales in TMEM
-          if (!ptx::mbar_wait(&full[stage], phase, p.wait_limit) ||
-              !ptx::mbar_wait(&sf_full[stage], phase, p.wait_limit)) {
+          // both CTAs' operand tiles in SMEM, both CTAs' scales in TMEM (one barrier)
+          if (!ptx::mbar_wait(&full[stage], phase, p.wait_limit)) {
             atomicExch(p.err, kErrMma);
             ok = false;
             break;
@@ -407,7 +406,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         ptx::tmem_st_wait();
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&sf_full[stage]), 0));
+        if (lane == 0) ptx::mbar_arrive_cluster(ptx::mapa(ptx::smem_u32(&full[stage]), 0));
         if (++stage == STAGES) {
           stage = 0;
           phase ^= 1u;
