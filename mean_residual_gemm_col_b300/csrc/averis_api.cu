@@ -418,6 +418,12 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
   for (int e = 0; e < ng; ++e)
     if (gs[e].rows > 0) tiles_all += cdiv(gs[e].rows, kQTile) * cdiv(C, kQTile);
   const int64_t budget = kQCtasPerSm * (int64_t)dev->sms;  // tile CTAs of one wave, shared out by tiles
+  // rank-one work of all groups: the mean CTAs of a launch take at most a
+  // quarter of a wave, shared out by the groups' weight rows (one each at
+  // least), so that mean and tile CTAs stay one resident wave
+  int64_t w_rows_all = 0;
+  for (int e = 0; e < ng; ++e)
+    if (gs[e].rows > 0 && gs[e].r_w != nullptr) w_rows_all += gs[e].r_w->rows;
   long long starve = 0;
   {
     std::lock_guard<std::mutex> lock(g_mutex);
@@ -492,7 +498,8 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
         q.w_ld = averis_nvfp4_ld(C);
         q.w_kc = cdiv(C, 64);
         q.r_out = G.r_out;
-        q.mean_ctas = (int)std::max<int64_t>(1, std::min<int64_t>(8, cdiv(G.r_w->rows * C, (int64_t)1 << 19)));
+        q.mean_ctas =
+            (int)std::max<int64_t>(1, std::min<int64_t>(8, (budget / 4) * G.r_w->rows / std::max<int64_t>(1, w_rows_all)));
       }
     }
     const int64_t tiles = (int64_t)q.tiles_r * q.tiles_c;
