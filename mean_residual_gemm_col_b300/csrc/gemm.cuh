@@ -17,7 +17,7 @@
 // CTA loads its own 128 rows of A and its own 128 rows of B (half of the
 // tile's N), so every SM streams 32 KB of operands per 256-element K tile
 // instead of the 48 KB a one-CTA 128 x 256 tile needs, and the shared-memory
-// ring is deeper for the same capacity.  A launch runs up to G GEMMs (the
+// ring is deeper for the same capacity (5 stages).  A launch runs up to G GEMMs (the
 // dW and dX of a layer, or the experts of a grouped layer), each with its own
 // output type; every pair runs a contiguous range of work units (GEMM after
 // GEMM, tiles M fastest), the ranges cut by the host so that the pairs' K
@@ -106,7 +106,10 @@ struct GemmCfg {
   static constexpr int BN = 256;       // output columns per tile (the MMA's N)
   static constexpr int BNH = BN / 2;   // rows of B per CTA
   static constexpr int BKB = 128;      // bytes of codes per row per K tile (256 elements)
-  static constexpr int STAGES = SFB_FULL ? 4 : 5;
+  // 5 stages x (32 KB of operands + 6 KB of scales) per CTA: 160 KB of operands in
+  // flight per SM; the epilogue gets one staging box per warp and one buffer of
+  // vector entries to make room (4 stages left the MMAs waiting for operands)
+  static constexpr int STAGES = 5;
   static constexpr int A_BYTES = BM * BKB;
   static constexpr int B_BYTES = BNH * BKB;
   static constexpr int SFA_BYTES = 4 * 512;
@@ -115,15 +118,15 @@ struct GemmCfg {
   static constexpr int EPI_WARPS = 8;                  // 2 per TMEM lane quarter, each half of the columns
   static constexpr int EPI_COLS = BN / (EPI_WARPS / 4);  // accumulator columns per epilogue warp
   static constexpr int EPI_BUF = 32 * 128;             // one warp's 32 rows x 128 bytes
-  static constexpr int EPI_NBUF = 2;                   // staging boxes per epilogue warp (two stores in flight)
+  static constexpr int EPI_NBUF = 1;                   // staging boxes per epilogue warp
   static constexpr int EPI_BYTES = EPI_WARPS * EPI_NBUF * EPI_BUF;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_EPI = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int OFF_VEC = OFF_EPI + EPI_BYTES;  // [2 tile parities][col_add, col_vec][BN] floats
-  static constexpr int OFF_BAR = OFF_VEC + 2 * 2 * BN * 4;
+  static constexpr int OFF_VEC = OFF_EPI + EPI_BYTES;  // [col_add, col_vec][BN] floats of the current tile
+  static constexpr int OFF_BAR = OFF_VEC + 2 * BN * 4;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;    // + alignment slack
   // TMEM columns: the accumulator, then per stage 16 SFA columns + the SFB columns
   static constexpr int SF_BASE = BN;
@@ -440,9 +443,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const int row0 = mt * Cfg::PM + (int)cta * Cfg::BM + q * 32;
       const int row = row0 + lane;
       const float rterm = (has_outer && row < gg.M) ? gg.outer * __ldg(gg.row_vec + row) : 0.f;
-      // this tile's vector entries -> SMEM (double-buffered by tile parity: a warp
-      // reaches the next tile's writes only after every warp passed this barrier)
-      float* cadd_s = vec_base + (it & 1) * 2 * BN;
+      // this tile's vector entries -> SMEM (one buffer: the barrier at the end of
+      // the previous tile kept every warp from writing while another still read)
+      float* cadd_s = vec_base;
       float* cvec_s = cadd_s + BN;
       for (int c = et; c < BN; c += 32 * EPI_WARPS) {
         const int col = nt * BN + c;
@@ -555,6 +558,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           store_box(w, nt * BN + c);
         }
       }
+      epi_bar<EPI_WARPS>();  // every warp has read this tile's vector entries (one buffer)
     }
     if (lane == 0) ptx::bulk_wait<0>();
     __syncwarp();
