@@ -143,6 +143,15 @@ size_t averis_quantize_workspace_bytes(int64_t rows, int64_t cols, unsigned flag
  *  out_row   NVFP4 [rows, cols] of T_R blocked along cols (output, NULL to skip).
  *  out_col   NVFP4 [cols, rows] of T_R^T blocked along rows (output, NULL to skip).
  *  workspace device scratch of averis_quantize_workspace_bytes() bytes.
+ * Kernels: a column-statistics pass, then the quantize pass (plus a rotated-
+ * maximum pass under HADAMARD16).  With the environment variable
+ * AVERIS_SINGLE_READ_QUANTIZE=1 set when the library first sees the device,
+ * an input of at most 1024 tiles of 128 x 128 whose tiles all fit the
+ * resident CTAs' shared memory (two CTAs of three tiles per SM), without
+ * HADAMARD16, takes one cooperative launch instead, which reads x once.  Its
+ * mu may differ from the two-launch path's in the last bit (the compensated
+ * column sums are added in another order), and on the B300 it is no faster at
+ * the sizes measured, so it is off by default.
  * Errors: INVALID_ARG (cols % 16, shapes of the outputs, alignment),
  * WORKSPACE_TOO_SMALL, UNSUPPORTED_ARCH, CUDA.
  */
@@ -306,7 +315,8 @@ const char* averis_status_string(averis_status status);
  * Returns AVERIS_OK or AVERIS_ERR_TIMEOUT; *where (if not NULL) receives the
  * code of the wait that gave up:
  *   1 GEMM TMA producer, 2 GEMM MMA issuer, 3 GEMM epilogue, 4 GEMM drain,
- *   5 quantize pass (an input box or tile never arrived), 6 GEMM scale feed.
+ *   5 quantize pass (an input box or tile never arrived), 6 GEMM scale feed,
+ *   7 single-read quantize (a grid-wide wait for its other CTAs gave up).
  * The results of the calls that timed out are invalid.  When it reports a
  * timeout it also zeroes the control block of averis_quantize_noalloc's
  * scratch, whose callers cannot reach it.

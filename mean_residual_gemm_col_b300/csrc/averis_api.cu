@@ -2,6 +2,7 @@
 // encoding and kernel launches.  Declarations and per-call contracts are in
 // include/averis.h.
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <algorithm>
 #include <mutex>
@@ -34,6 +35,8 @@ struct DeviceInfo {
   int* err_word = nullptr;
   bool attrs_set = false;
   int gemm_pairs = 0;  // clusters of two GEMM CTAs resident at once (the persistent grid's size)
+  int resident_ctas = 0;  // CTAs of the single-read quantize resident at once (its cooperative grid)
+  bool resident_on = false;  // AVERIS_SINGLE_READ_QUANTIZE=1 turns the single-read quantize on
 };
 DeviceInfo g_dev[kMaxDevices];
 std::mutex g_mutex;
@@ -95,6 +98,13 @@ averis_status device_info(DeviceInfo** out) {
     if (cudaOccupancyMaxActiveClusters(&pairs, gemm_nvfp4_kernel<kSfbFull, 1>, &cfg) != cudaSuccess || pairs < 1)
       return AVERIS_ERR_CUDA;
     d.gemm_pairs = std::min(std::min(pairs, d.sms / 2), kMaxPairs);
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, quantize_resident_kernel, kQThreads, kQSmem) !=
+        cudaSuccess)
+      return AVERIS_ERR_CUDA;
+    d.resident_ctas = std::min(per_sm, kQCtasPerSm) * d.sms;
+    const char* env = std::getenv("AVERIS_SINGLE_READ_QUANTIZE");
+    d.resident_on = env != nullptr && env[0] == '1';
     d.attrs_set = true;
   }
   *out = &d;
@@ -111,6 +121,9 @@ averis_status set_attrs() {
       cudaSuccess)
     return AVERIS_ERR_CUDA;
   if (cudaFuncSetAttribute(split_quant_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
+      cudaSuccess)
+    return AVERIS_ERR_CUDA;
+  if (cudaFuncSetAttribute(quantize_resident_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem) !=
       cudaSuccess)
     return AVERIS_ERR_CUDA;
   if (cudaFuncSetAttribute(colstats_grouped_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStatsSmem) !=
@@ -164,9 +177,18 @@ StatsGeom stats_geom(int64_t R, int64_t C) {
 constexpr size_t kCtrlBytes = ((size_t)kCtrlWords * sizeof(unsigned) + 255) & ~size_t(255);
 static_assert(kCtrlBytes == AVERIS_WORKSPACE_CTRL_BYTES, "control block size is part of the ABI");
 
+// The single-read quantize keeps every 128 x 128 tile of X in shared memory
+// (kQBufs per CTA, kQCtasPerSm CTAs per SM): tensors of at most this many
+// tiles may take it (888 on a 148-SM part), and their workspace holds one
+// row of column partials per tile row (at most 2 KB per tile).
+constexpr int64_t kResidentMaxTiles = 1024;
+
+bool resident_size(int64_t R, int64_t C) { return cdiv(R, kQTile) * cdiv(C, kQTile) <= kResidentMaxTiles; }
+
 size_t quant_ws_bytes(int64_t R, int64_t C) {
   const StatsGeom g = stats_geom(R, C);
-  return kCtrlBytes + align256((size_t)g.nrb * (size_t)C * sizeof(ColPartial));
+  const int64_t rows = resident_size(R, C) ? std::max<int64_t>(g.nrb, cdiv(R, kQTile)) : g.nrb;
+  return kCtrlBytes + align256((size_t)rows * (size_t)C * sizeof(ColPartial));
 }
 
 // Launch with programmatic stream serialization: the kernel may start while
@@ -185,6 +207,26 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// The same with a cooperative launch: every CTA of the grid is resident at
+// once (the single-read quantize waits grid-wide, bounded).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_coop_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeCooperative;
+  attr[1].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 
@@ -269,8 +311,6 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   if (!encode_2d(&tstats, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x), (uint64_t)C, (uint64_t)R,
                  (uint64_t)C * 2, 64u, (uint32_t)kStatsBoxRows))
     return AVERIS_ERR_CUDA;
-  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
-    return AVERIS_ERR_CUDA;
 
   // The quantize pass also writes the NVFP4 mean (one of its CTAs) and resets
   // the control block, so it runs even with no residual layout requested.
@@ -337,6 +377,33 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
   // all CTAs resident at once (2 per SM): tile CTAs fill what the mean CTAs leave
   const int tile_ctas =
       ntiles == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(ntiles, kQCtasPerSm * (int64_t)dev->sms - qp.mean_ctas));
+  // opt-in: a tensor whose tiles all fit the resident CTAs' buffers (and no
+  // rotation, which needs the rotated maxima before any tile is quantized) in
+  // one cooperative launch that reads X once.  Measured on a B300 at 8192 x
+  // 1024 it takes as long as the two launches (20.1 against 20.4 us in a CUDA
+  // graph): the pass is bound by its arithmetic and fixed latencies, not by the
+  // second read of X (from L2), and its two grid-wide waits cost what the
+  // saved launch gains
+
+  const int64_t tile_slots = (int64_t)(dev->resident_ctas - qp.mean_ctas) * kQBufs;
+  if (dev->resident_on && !had && ntiles > 0 && ntiles <= kResidentMaxTiles && ntiles <= tile_slots &&
+      ws_bytes >= kCtrlBytes + (size_t)qp.tiles_r * (size_t)C * sizeof(ColPartial)) {
+    ResidentParams rp{};
+    rp.q = qp;
+    rp.mu = split ? mu : nullptr;
+    rp.part = part;
+    rp.grid_wait_limit = kWaitLimit;
+    if (sp.starve) {
+      rp.starve = 1;
+      rp.q.wait_limit = sp.wait_limit;
+    }
+    if (launch_coop_pdl(quantize_resident_kernel, dim3(dev->resident_ctas), dim3(kQThreads), kQSmem, s, tx, rp) !=
+        cudaSuccess)
+      return AVERIS_ERR_CUDA;
+    return AVERIS_OK;
+  }
+  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
+    return AVERIS_ERR_CUDA;
   if (had) {
     QuantParams ap = qp;  // rotated-maximum pass: tiles only
     ap.mean_ctas = 0;

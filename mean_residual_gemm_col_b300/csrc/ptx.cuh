@@ -339,7 +339,8 @@ enum : int {
   kErrEpilogue = 3,   // GEMM epilogue: accumulator never completed
   kErrDrain = 4,      // GEMM: own tensor-core work did not complete
   kErrQuantLoad = 5,  // quantize pass: an input tile never arrived
-  kErrScaleFeed = 6   // GEMM scale warps: a stage's operands never arrived
+  kErrScaleFeed = 6,  // GEMM scale warps: a stage's operands never arrived
+  kErrQuantGrid = 7   // single-read quantize: a grid-wide wait for the other CTAs gave up
 };
 
 constexpr long long kWaitLimit = 1ll << 31;  // ~1 s of SM clock

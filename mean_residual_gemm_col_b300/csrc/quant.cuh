@@ -39,6 +39,7 @@ enum : int {
   kCtrlAmaxRowH = 5,     // rotated residual max, layout blocked along columns (Hadamard)
   kCtrlAmaxColH = 6,     // rotated residual max, layout blocked along rows (Hadamard)
   kCtrlQuantTicket = 7,  // quantize pass: CTAs finished
+  kCtrlGridBar = 9,      // single-read quantize: arrivals at its grid-wide waits
   kCtrlStrip = 64,       // per-strip-group tickets of the stats pass
   kMaxStripGroups = 1024,
   kCtrlWords = kCtrlStrip + kMaxStripGroups
@@ -1092,6 +1093,313 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
   int e = 0;
   while (e + 1 < gp.ngroups && gp.cta0[e + 1] <= (int)blockIdx.x) ++e;
   split_quant_body<AMAX_ONLY, HAD>(tmX, gp.g[e], (int)blockIdx.x - gp.cta0[e], gp.cta0[e + 1] - gp.cta0[e]);
+}
+
+// ------------------------------------------------ single-read quantize ----
+//
+// For inputs whose 128 x 128 tiles all fit the tile buffers of one wave of
+// CTAs (2 per SM x kQBufs each: about 29 MB of bf16 on a B300), one
+// cooperative launch reads every tile of X from HBM once and keeps it in
+// shared memory: (1) column partials of each resident tile (compensated sum,
+// max, min) into the workspace; a grid-wide wait; (2) each CTA combines a
+// share of the columns (the same binary32 hi + lo arithmetic as the stats
+// pass) into mu and the residual's maximum magnitude; a grid-wide wait; (3)
+// the quantize pass of the two-launch path, tile by tile, from the resident
+// tiles, with the mean CTAs quantizing the mean and computing the rank-one
+// row.  Grid-wide waits count arrivals in the control block, bounded; the
+// last CTA resets the words.  No rotation (the Hadamard variant needs the
+// rotated maxima first and keeps the two-launch path).
+
+struct ResidentParams {
+  QuantParams q;     // the quantize pass's parameters (outputs, mean, rank-one row, control block)
+  float* mu;         // [C] out (split; q.mu is the same pointer), null without the split
+  ColPartial* part;  // [tiles_r][C] column partials of each tile
+  long long grid_wait_limit;  // bound of each grid-wide wait, in SM clock cycles
+  int starve;        // diagnostics only: request no tiles, so that every wait for one runs out
+};
+
+// the column partials of one tile ([4 row quarters][128 columns] float4) reuse
+// the mean / table / staging area, which the quantize phase fills only later
+static_assert(kQOffMu + 4 * 128 * 16 <= kQOffBar, "tile partials do not fit the staging area");
+
+// Column partials of one resident tile (all 256 threads): thread t sums the
+// column pair 2(t % 64), 2(t % 64) + 1 over rows 32(t / 64) .. +31 (groups of 8
+// rows added pairwise, then compensated, as in the stats pass); the four row
+// quarters are combined as hi + lo pairs in a fixed order.  Rows at or past R
+// count neither in the sum nor in the extremes.
+__device__ __forceinline__ void resident_tile_stats(const uint8_t* buf, float4* scratch, int64_t r0, int64_t c0,
+                                                    int64_t R, int64_t C, ColPartial* part_row) {
+  const int tid = threadIdx.x;
+  const int cp = tid & 63, rq = tid >> 6;
+  const uint8_t* hb = buf + (cp >> 5) * kQHalf;
+  const int w = cp & 31;  // word of the column pair in the 128-byte box row
+  const int64_t rows_left = R - r0;
+  uint64_t s2 = 0ull, c2 = 0ull;
+  uint32_t mx2 = 0xFF80FF80u, mn2 = 0x7F807F80u;  // -inf, +inf
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    uint32_t xs[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int row = 32 * rq + 8 * g + j;
+      const uint32_t v = *reinterpret_cast<const uint32_t*>(hb + row * 128 + ((((w >> 2) ^ (row & 7))) << 4) + 4 * (w & 3));
+      const bool valid = row < rows_left;
+      mx2 = bmax2(mx2, valid ? v : 0xFF80FF80u);
+      mn2 = bmin2(mn2, valid ? v : 0x7F807F80u);
+      xs[j] = valid ? v : 0u;  // +0 + +0: adds nothing
+    }
+    const uint64_t t = add2(add2(add2(bf2_to_f2(xs[0]), bf2_to_f2(xs[1])), add2(bf2_to_f2(xs[2]), bf2_to_f2(xs[3]))),
+                            add2(add2(bf2_to_f2(xs[4]), bf2_to_f2(xs[5])), add2(bf2_to_f2(xs[6]), bf2_to_f2(xs[7]))));
+    const uint64_t y = sub2(t, c2);
+    const uint64_t tt = add2(s2, y);
+    c2 = sub2(sub2(tt, s2), y);
+    s2 = tt;
+  }
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const float sv = h ? f2hi(s2) : f2lo(s2), cv = h ? f2hi(c2) : f2lo(c2);
+    const F2 d = fast_two_sum(sv, -cv);
+    scratch[rq * 128 + 2 * cp + h] =
+        make_float4(d.hi, d.lo, h ? bf16hi(mx2) : bf16lo(mx2), h ? bf16hi(mn2) : bf16lo(mn2));
+  }
+  __syncthreads();
+  if (tid < 128 && c0 + tid < C) {
+    float4 q = scratch[tid];
+    F2 acc{q.x, q.y};
+    float m1 = q.z, m2 = q.w;
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+      q = scratch[k * 128 + tid];
+      acc = df_add(acc, F2{q.x, q.y});
+      m1 = fmaxf(m1, q.z);
+      m2 = fminf(m2, q.w);
+    }
+    *reinterpret_cast<float4*>(part_row + c0 + tid) = make_float4(acc.hi, acc.lo, m1, m2);
+  }
+  __syncthreads();  // scratch is free for the next tile
+}
+
+// Columns [c_begin, c_end) of the tiles' partials -> mu (split) and this
+// CTA's share of the residual's maximum magnitude.  One warp per column:
+// lanes add the tile rows lane, lane + 32, ... in order, then a fixed
+// butterfly over the lanes.  All 256 threads call it; returns the maximum
+// (valid in every thread).
+__device__ __forceinline__ float resident_combine(const QuantParams& p, const ColPartial* part, float* mu_out,
+                                                  int64_t c_begin, int64_t c_end, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int tiles_r = p.tiles_r;
+  const float Rf = (float)p.R;
+  float a_res = 0.f;
+  for (int64_t c = c_begin + warp; c < c_end; c += 8) {
+    F2 acc{0.f, 0.f};
+    float m1 = -FLT_MAX, m2 = FLT_MAX;
+    for (int j = lane; j < tiles_r; j += 32) {
+      const float4 q = __ldcg(reinterpret_cast<const float4*>(part + (int64_t)j * p.C + c));
+      acc = df_add(acc, F2{q.x, q.y});
+      m1 = fmaxf(m1, q.z);
+      m2 = fminf(m2, q.w);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const F2 other{__shfl_xor_sync(0xffffffffu, acc.hi, o), __shfl_xor_sync(0xffffffffu, acc.lo, o)};
+      acc = (lane & o) ? df_add(other, acc) : df_add(acc, other);
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      m2 = fminf(m2, __shfl_xor_sync(0xffffffffu, m2, o));
+    }
+    if (mu_out != nullptr) {
+      const float mu = df_div_count(acc, Rf);
+      if (lane == 0) mu_out[c] = mu;
+      a_res = fmaxf(a_res, fmaxf(fabsf(__fsub_rn(m1, mu)), fabsf(__fsub_rn(m2, mu))));
+    } else {
+      a_res = fmaxf(a_res, fmaxf(fabsf(m1), fabsf(m2)));
+    }
+  }
+  return block_max256(a_res, red);
+}
+
+__device__ __forceinline__ unsigned ld_acquire_gpu(const unsigned* a) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(a) : "memory");
+  return v;
+}
+
+// Grid-wide wait of the single-read quantize: every CTA adds one to the
+// control word, then (when `wait`) waits until `target` arrivals are counted.
+// A CTA that has already given up still arrives, so that the others are not
+// held until their own limit.  Returns false (uniform over the CTA) when the
+// wait ran out.
+__device__ __forceinline__ bool resident_grid_wait(unsigned* ctrl, unsigned target, bool wait, long long limit,
+                                                   int* s_ok) {
+  __syncthreads();  // this CTA's writes are issued
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(&ctrl[kCtrlGridBar], 1u);
+    int ok = 1;
+    if (wait) {
+      const long long t0 = clock64();
+      while (ld_acquire_gpu(&ctrl[kCtrlGridBar]) < target) {
+        if (clock64() - t0 > limit) {
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+      __threadfence();
+    }
+    *s_ok = ok;
+  }
+  __syncthreads();
+  return *s_ok != 0;
+}
+
+__global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
+    quantize_resident_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ ResidentParams rp) {
+  const QuantParams& p = rp.q;
+  extern __shared__ uint8_t qraw[];
+  uint8_t* sm = qraw + ((1024u - (ptx::smem_u32(qraw) & 1023u)) & 1023u);  // stays a shared-space pointer
+  float* mu_s = reinterpret_cast<float*>(sm + kQOffMu);
+  float* inv_s = reinterpret_cast<float*>(sm + kQOffInv);
+  float4* scratch = reinterpret_cast<float4*>(sm + kQOffMu);  // column partials of a tile, before mu_s is used
+  uint64_t* full = reinterpret_cast<uint64_t*>(sm + kQOffBar);
+  __shared__ float red[8];
+  __shared__ int s_ok, s_last;
+
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int cta = blockIdx.x, ncta = gridDim.x;
+  const int ntiles = p.tiles_r * p.tiles_c;
+  const bool split = rp.mu != nullptr;
+  const bool mean_cta = cta < p.mean_ctas;
+  const int tcta = cta - p.mean_ctas, ntcta = ncta - p.mean_ctas;  // tile CTA index, count
+  int nmine = 0;  // this CTA's tiles: tcta, tcta + ntcta, ... (buffer k holds the k-th)
+  if (!mean_cta)
+    while (nmine < kQBufs && tcta + nmine * ntcta < ntiles) ++nmine;
+
+  if (tid == 0) {
+    for (int b = 0; b < kQBufs; ++b) ptx::mbar_init(&full[b], 1);
+    ptx::fence_mbar_init();
+    ptx::prefetch_tmap(&tmX);
+  }
+  __syncthreads();
+  // X may come from the kernel just before this one: load it after the wait
+  ptx::pdl_wait_and_release();
+  if (tid == 0 && !rp.starve) {
+    const uint64_t once = ptx::l2_policy_evict_first();  // the only read of X
+    for (int k = 0; k < nmine; ++k) {
+      const int tile = tcta + k * ntcta;
+      const int32_t x0 = (tile % p.tiles_c) * kQTile, y = (tile / p.tiles_c) * kQTile;
+      ptx::mbar_arrive_expect_tx(&full[k], (uint32_t)kQTileBytes);
+      ptx::tma_load_2d_hint(sm + k * kQTileBytes, &tmX, x0, y, &full[k], once);
+      ptx::tma_load_2d_hint(sm + k * kQTileBytes + kQHalf, &tmX, x0 + 64, y, &full[k], once);
+    }
+  }
+
+  // (1) column partials of each resident tile
+  bool failed = false;
+  int landed = 0;  // tiles known to have arrived
+  for (; landed < nmine; ++landed) {
+    if (!__syncthreads_and(ptx::mbar_wait(&full[landed], 0u, p.wait_limit) ? 1 : 0)) {
+      if (tid == 0) atomicExch(p.err, kErrQuantLoad);
+      failed = true;
+      break;
+    }
+    const int tile = tcta + landed * ntcta;
+    const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
+    resident_tile_stats(sm + landed * kQTileBytes, scratch, (int64_t)tr * kQTile, (int64_t)tc * kQTile, p.R, p.C,
+                        rp.part + (int64_t)tr * p.C);
+  }
+  if (!resident_grid_wait(p.ctrl, (unsigned)ncta, !failed, rp.grid_wait_limit, &s_ok) && !failed) {
+    if (tid == 0) atomicCAS(p.err, 0, kErrQuantGrid);  // keep the cause if another CTA reported one
+    failed = true;
+  }
+
+  // (2) mu and the residual's maximum over this CTA's share of the columns
+  if (!failed) {
+    const int64_t per = (p.C + ncta - 1) / ncta;
+    const int64_t c_begin = min(p.C, (int64_t)cta * per), c_end = min(p.C, c_begin + per);
+    const float a_res = resident_combine(p, rp.part, rp.mu, c_begin, c_end, red);
+    if (tid == 0) atomicMax(&p.ctrl[kCtrlAmaxRes], __float_as_uint(a_res));
+  }
+  if (!resident_grid_wait(p.ctrl, 2u * (unsigned)ncta, !failed, rp.grid_wait_limit, &s_ok) && !failed) {
+    if (tid == 0) atomicCAS(p.err, 0, kErrQuantGrid);
+    failed = true;
+  }
+
+  // (3) the quantize pass over the resident tiles, the mean and the rank-one row
+  if (!failed) {
+    const float amax = __uint_as_float(__ldcg(&p.ctrl[kCtrlAmaxRes]));
+    const float s_g = tensor_scale_of(amax);  // one tensor scale for both layouts (no rotation)
+    if (tid < 128) {
+      const float inv = tid < 127 ? inv_scale_of(tid, s_g) : 0.f;
+      inv_s[tid] = inv;
+      inv_s[128 + tid] = inv;
+    }
+    if (cta == 0 && tid == 0) {
+      if (p.row_ts) *p.row_ts = s_g;
+      if (p.col_ts) *p.col_ts = s_g;
+    }
+    for (int k = 0; k < nmine; ++k) {
+      const int64_t c0 = (int64_t)((tcta + k * ntcta) % p.tiles_c) * kQTile;
+      if (tid < 128) mu_s[128 * k + tid] = split && c0 + tid < p.C ? __ldcg(rp.mu + c0 + tid) : 0.f;  // x - 0 = x
+    }
+    __syncthreads();
+    if (split && mean_cta) {
+      uint8_t* s_codes = sm;  // a mean CTA holds no tiles
+      uint8_t* s_scales = sm + kQOffMu - kQBufs * kQTileBytes / 4;
+      const float s_mu = quantize_mean(p, cta == 0, s_codes, s_scales, red);
+      if (p.r_out != nullptr) {
+        const int64_t per = (p.w_rows + p.mean_ctas - 1) / p.mean_ctas;
+        const int64_t n0 = (int64_t)cta * per;
+        rank1_rows(p, n0, min(p.w_rows, n0 + per), s_codes, s_scales, s_mu);
+      }
+    }
+    const float den = __fmul_rn(6.0f, s_g);
+    const bool rows_on = p.row_codes != nullptr, cols_on = p.col_codes != nullptr;
+    float unused_r = 0.f, unused_c = 0.f;
+    for (int k = 0; k < nmine; ++k) {
+      const int tile = tcta + k * ntcta;
+      const int64_t r0 = (int64_t)(tile / p.tiles_c) * kQTile, c0 = (int64_t)(tile % p.tiles_c) * kQTile;
+      const uint8_t* buf = sm + k * kQTileBytes;
+      uint8_t* stage = sm + kQOffStage + k * kQStageBytes;
+      if (r0 + kQTile > p.R || c0 + kQTile > p.C)
+        quant_tile_warp<false, false, true>(p, buf, mu_s + 128 * k, stage, r0, c0, den, den, s_g > 0.f, s_g > 0.f,
+                                            inv_s, rows_on, cols_on, unused_r, unused_c);
+      else
+        quant_tile_warp<false, false, false>(p, buf, mu_s + 128 * k, stage, r0, c0, den, den, s_g > 0.f, s_g > 0.f,
+                                             inv_s, rows_on, cols_on, unused_r, unused_c);
+    }
+    __syncthreads();  // every warp's scale atoms are staged
+    // 4 atoms x 512 B per tile: row layout (row chunk tr, column chunks 2tc,
+    // 2tc+1), column layout (row chunk tc, column chunks 2tr, 2tr+1)
+    for (int a = warp; a < 4 * nmine; a += kQWarps) {
+      const int k = a >> 2, tile = tcta + k * ntcta;
+      const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
+      const bool is_col = (a & 2) != 0;
+      const int64_t kc = (is_col ? 2 * (int64_t)tr : 2 * (int64_t)tc) + (a & 1);
+      const bool on = is_col ? (cols_on && kc < p.col_kc) : (rows_on && kc < p.row_kc);
+      if (on) {
+        uint8_t* dst = is_col ? p.col_scales + ((int64_t)tc * p.col_kc + kc) * 512
+                              : p.row_scales + ((int64_t)tr * p.row_kc + kc) * 512;
+        *reinterpret_cast<uint4*>(dst + 16 * lane) =
+            *reinterpret_cast<const uint4*>(sm + kQOffStage + k * kQStageBytes + 512 * (a & 3) + 16 * lane);
+      }
+    }
+  }
+
+  // (4) a CTA that gave up lets the tiles it requested land (bounded) before
+  // its shared memory is given up; the last CTA resets the control words
+  if (failed && tid == 0 && !rp.starve)
+    for (int k = landed; k < nmine; ++k) ptx::mbar_wait(&full[k], 0u, p.wait_limit);
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned t = atomicAdd(&p.ctrl[kCtrlQuantTicket], 1u);
+    s_last = (t == (unsigned)ncta - 1);
+    if (s_last) {
+      p.ctrl[kCtrlAmaxRes] = 0u;
+      p.ctrl[kCtrlGridBar] = 0u;
+      p.ctrl[kCtrlQuantTicket] = 0u;
+    }
+  }
 }
 
 // --------------------------------------------------------- rank-one GEMV --
