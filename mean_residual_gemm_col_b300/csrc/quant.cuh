@@ -106,6 +106,21 @@ __device__ __forceinline__ uint64_t bf_pair_sub(uint32_t wa, uint32_t wb, bool h
         : "r"(wa), "r"(wb), "f"(m));
   return f2pack(d0, d1);
 }
+// (fl32(bf16 a - ma), fl32(bf16 b - mb)) of one half (hi: the upper one) of each of two words.
+__device__ __forceinline__ uint64_t bf_pair_sub2(uint32_t wa, uint32_t wb, bool hi, float ma, float mb) {
+  float d0, d1;
+  if (hi)
+    asm("{\n .reg .b16 l0, h0, l1, h1;\n mov.b32 {l0, h0}, %2;\n mov.b32 {l1, h1}, %3;\n"
+        " sub.rn.f32.bf16 %0, h0, %4;\n sub.rn.f32.bf16 %1, h1, %5;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(wa), "r"(wb), "f"(ma), "f"(mb));
+  else
+    asm("{\n .reg .b16 l0, h0, l1, h1;\n mov.b32 {l0, h0}, %2;\n mov.b32 {l1, h1}, %3;\n"
+        " sub.rn.f32.bf16 %0, l0, %4;\n sub.rn.f32.bf16 %1, l1, %5;\n}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(wa), "r"(wb), "f"(ma), "f"(mb));
+  return f2pack(d0, d1);
+}
 // The two bf16 values of a packed word as a binary32 pair (exact).
 __device__ __forceinline__ uint64_t bf2_to_f2(uint32_t w) { return f2pack(bf16lo(w), bf16hi(w)); }
 // Element-wise max / min of two packed bf16 pairs (exact).
@@ -172,6 +187,35 @@ __device__ __forceinline__ void fwht16(float (&v)[16]) {
   }
 #pragma unroll
   for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+// The same butterfly on packed pairs, for the tile quantizer: on entry
+// p[k] = (v[k], v[k+8]), k < 8.  Strides 1, 2 and 4 pair whole registers
+// (packed adds and subtractions), stride 8 pairs the two halves of each
+// register; on exit p[m] = (v[2m], v[2m+1]) * 1/4.  Every element sees the
+// same binary32 operations in the same order as fwht16.
+__device__ __forceinline__ void fwht16_x2(uint64_t (&p)[8]) {
+#pragma unroll
+  for (int h = 1; h < 8; h <<= 1) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      if (!(k & h)) {
+        const uint64_t a = p[k], b = p[k + h];
+        p[k] = add2(a, b);
+        p[k + h] = sub2(a, b);
+      }
+    }
+  }
+  float o[16];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float a = f2lo(p[k]), b = f2hi(p[k]);
+    o[k] = __fadd_rn(a, b);
+    o[k + 8] = __fsub_rn(a, b);
+  }
+  const uint64_t quarter = f2pack(0.25f, 0.25f);
+#pragma unroll
+  for (int m = 0; m < 8; ++m) p[m] = mul2(f2pack(o[2 * m], o[2 * m + 1]), quarter);
 }
 
 struct BlockQ {
@@ -821,19 +865,37 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
       const uint4 v0 = *reinterpret_cast<const uint4*>(hb + row * 128 + (((2 * kb) ^ (row & 7)) << 4));
       const uint4 v1 = *reinterpret_cast<const uint4*>(hb + row * 128 + (((2 * kb + 1) ^ (row & 7)) << 4));
       const uint32_t wv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-      float rx[16];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint64_t d = bf2_sub_f2(wv[e], m2[e]);
-        rx[2 * e] = f2lo(d);
-        rx[2 * e + 1] = f2hi(d);
-      }
       const bool valid = !EDGE || (cvalid && gr < p.R);
-      if (EDGE && !valid) {
+      float rx[16];
+      if constexpr (HAD) {
+        // residual pairs (k, k + 8), then the packed butterfly
+        uint64_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) rx[e] = 0.f;
+        for (int k = 0; k < 8; ++k) {
+          const int e = k >> 1;
+          const bool h = (k & 1) != 0;
+          pk[k] = bf_pair_sub2(wv[e], wv[e + 4], h, h ? f2hi(m2[e]) : f2lo(m2[e]),
+                               h ? f2hi(m2[e + 4]) : f2lo(m2[e + 4]));
+          if (EDGE && !valid) pk[k] = 0ull;
+        }
+        fwht16_x2(pk);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          rx[2 * e] = f2lo(pk[e]);
+          rx[2 * e + 1] = f2hi(pk[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint64_t d = bf2_sub_f2(wv[e], m2[e]);
+          rx[2 * e] = f2lo(d);
+          rx[2 * e + 1] = f2hi(d);
+        }
+        if (EDGE && !valid) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) rx[e] = 0.f;
+        }
       }
-      if (HAD) fwht16(rx);
       if (AMAX_ONLY) {
         amax_row = fmaxf(amax_row, absmax16(rx));
       } else {
@@ -858,23 +920,44 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
     const int64_t off = (r0 + row0) / 2;  // code byte offset of the block within a column
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float rx[16];
-#pragma unroll
-      for (int e = 0; e < 16; e += 2) {
-        const uint32_t wa = (j >> 1) ? x[e].y : x[e].x;
-        const uint32_t wb = (j >> 1) ? x[e + 1].y : x[e + 1].x;
-        const uint64_t d = bf_pair_sub(wa, wb, (j & 1) != 0, mc[j]);
-        rx[e] = f2lo(d);
-        rx[e + 1] = f2hi(d);
-      }
       const int cc = 64 * half + 4 * cq + j;  // tile column
       const bool cvalid = !EDGE || c0 + cc < p.C;
-      if (EDGE) {
+      float rx[16];
+      if constexpr (HAD) {
+        // residual pairs (rows k, k + 8), then the packed butterfly
+        uint64_t pk[8];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          if (!cvalid || r0 + row0 + e >= p.R) rx[e] = 0.f;
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t wa = (j >> 1) ? x[k].y : x[k].x;
+          const uint32_t wb = (j >> 1) ? x[k + 8].y : x[k + 8].x;
+          pk[k] = bf_pair_sub(wa, wb, (j & 1) != 0, mc[j]);
+          if (EDGE) {
+            const float lo = !cvalid || r0 + row0 + k >= p.R ? 0.f : f2lo(pk[k]);
+            const float hi = !cvalid || r0 + row0 + k + 8 >= p.R ? 0.f : f2hi(pk[k]);
+            pk[k] = f2pack(lo, hi);
+          }
+        }
+        fwht16_x2(pk);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          rx[2 * e] = f2lo(pk[e]);
+          rx[2 * e + 1] = f2hi(pk[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; e += 2) {
+          const uint32_t wa = (j >> 1) ? x[e].y : x[e].x;
+          const uint32_t wb = (j >> 1) ? x[e + 1].y : x[e + 1].x;
+          const uint64_t d = bf_pair_sub(wa, wb, (j & 1) != 0, mc[j]);
+          rx[e] = f2lo(d);
+          rx[e + 1] = f2hi(d);
+        }
+        if (EDGE) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (!cvalid || r0 + row0 + e >= p.R) rx[e] = 0.f;
+        }
       }
-      if (HAD) fwht16(rx);
       if (AMAX_ONLY) {
         amax_col = fmaxf(amax_col, absmax16(rx));
       } else {
