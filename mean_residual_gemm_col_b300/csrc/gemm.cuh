@@ -270,12 +270,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           if (rba < gg.rb_a)
             ptx::bulk_load(smem + Cfg::OFF_SFA + stage * Cfg::SFA_BYTES,
                            gg.sfa + ((int64_t)rba * gg.kc + 4 * kt) * 512, ns * 512u, &sf_loaded[stage]);
-#pragma unroll
-          for (int h = 0; h < Cfg::SFB_HALVES; ++h) {
-            const int rb = nt * 2 + (SFB_FULL ? h : (int)cta);
+          if constexpr (SFB_FULL) {
+            // both CTAs need the scales of all 256 B rows: each loads the half of
+            // its own B rows once, multicast to both (the partner's stage slot is
+            // free: the commit that freed this stage here freed it there too, after
+            // both CTAs' scale warps had read it)
+            const int rb = nt * 2 + (int)cta;
             if (rb < gg.rb_b)
-              ptx::bulk_load(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES + h * 2048,
-                             gg.sfb + ((int64_t)rb * gg.kc + 4 * kt) * 512, ns * 512u, &sf_loaded[stage]);
+              ptx::bulk_load_mc(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES + (int)cta * 2048,
+                                gg.sfb + ((int64_t)rb * gg.kc + 4 * kt) * 512, ns * 512u, &sf_loaded[stage], 0x3);
+          } else {
+            const int rb = nt * 2 + (int)cta;
+            if (rb < gg.rb_b)
+              ptx::bulk_load(smem + Cfg::OFF_SFB + stage * Cfg::SFB_BYTES, gg.sfb + ((int64_t)rb * gg.kc + 4 * kt) * 512,
+                             ns * 512u, &sf_loaded[stage]);
           }
           // both CTAs' operand halves complete on the leader's stage barrier
           const uint32_t full_leader = ptx::mapa(ptx::smem_u32(&full[stage]), 0);
