@@ -48,7 +48,7 @@ CPU_SAMPLE_TOKENS = 256
 # launches that the per-kernel timing replays (NVTX range gemm_group_timed) in
 # one ncu capture, keyed by a hash of the GEMM source the capture was taken
 # on; any other source reports null.
-GEMM_TRAFFIC = {"401f6b50a3ba6bea": 245.31e6 / 12}
+GEMM_TRAFFIC = {"c5223afa2900bdb6": 244.57e6 / 12}
 
 
 def gemm_traffic_per_launch():
@@ -620,6 +620,7 @@ def run_ours(args, rank, ws):
         del graphs, ggraphs
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
+        line["gemm_alone"] = gemm_alone(fp4_peak)
         line["quantize_sweep"] = quantize_sweep(peaks)
         line["preprocess_vs_hadamard"] = preprocess_comparison()
         line["stack_28_layers"] = stack_comparison()
@@ -696,6 +697,35 @@ def quantize_sweep(peaks, iters=5):
             del x, run, keep
     torch.cuda.empty_cache()
     return out
+
+
+def gemm_alone(fp4_peak, n=8192, iters=9):
+    """One NVFP4 GEMM of n x n x n (bf16 output, no epilogue terms) through
+    averis_gemm, its operands quantized from seeded synthetic activations;
+    median device time over single launches with L2 flushed before each."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    dev = torch.device("cuda", torch.cuda.current_device())
+    ops = []
+    for seed in (1, 2):
+        x = workloads.torch_activation(seed, n, n, spike=30.0, device=dev)
+        ops.append(capi.averis_quantize(x, 0, want_col=False)["row"])
+        del x
+    out = torch.empty(n, n, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def run():
+        capi.averis_gemm(ops[0], ops[1], out_bf16=True, out=out)
+
+    run()
+    torch.cuda.synchronize()
+    ms = _time_each(run, iters, flush, torch.cuda.current_stream())
+    tflops = 2.0 * n ** 3 / (ms * 1e-3) / 1e12
+    del ops, out, flush
+    torch.cuda.empty_cache()
+    return {"m": n, "n": n, "k": n, "us": round(ms * 1e3, 1), "tflops": round(tflops, 1),
+            "fp4_peak_frac": round(tflops / fp4_peak, 4), "l2": "flushed before each launch"}
 
 
 def preprocess_comparison(iters=3):
