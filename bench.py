@@ -699,33 +699,57 @@ def quantize_sweep(peaks, iters=5):
     return out
 
 
-def gemm_alone(fp4_peak, n=8192, iters=9):
+def gemm_alone(fp4_peak, n=8192, sets=3, reps=10, iters=9):
     """One NVFP4 GEMM of n x n x n (bf16 output, no epilogue terms) through
-    averis_gemm, its operands quantized from seeded synthetic activations;
-    median device time over single launches with L2 flushed before each."""
+    averis_gemm, its operands quantized from seeded synthetic activations.
+    Timed two ways: back to back in a CUDA graph over `sets` operand pairs taken
+    in turn (226 MB of operands for n = 8192, more than L2, so each launch
+    streams its operands from HBM), and as the median of single launches with
+    L2 flushed (overwritten) before each."""
     import torch
     from mean_residual_gemm_col_b300 import capi
 
     dev = torch.device("cuda", torch.cuda.current_device())
     ops = []
-    for seed in (1, 2):
-        x = workloads.torch_activation(seed, n, n, spike=30.0, device=dev)
-        ops.append(capi.averis_quantize(x, 0, want_col=False)["row"])
-        del x
+    for k in range(sets):
+        pair = []
+        for seed in (2 * k + 1, 2 * k + 2):
+            x = workloads.torch_activation(seed, n, n, spike=30.0, device=dev)
+            pair.append(capi.averis_quantize(x, 0, want_col=False)["row"])
+            del x
+        ops.append(pair)
     out = torch.empty(n, n, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def run():
-        capi.averis_gemm(ops[0], ops[1], out_bf16=True, out=out)
+    def run_all():
+        for a, b in ops:
+            capi.averis_gemm(a, b, out_bf16=True, out=out)
 
-    run()
+    run_all()
     torch.cuda.synchronize()
-    ms = _time_each(run, iters, flush, torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        run_all()
+    g.replay()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(reps):
+        g.replay()
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / (reps * sets)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ms_flush = _time_each(lambda: capi.averis_gemm(ops[0][0], ops[0][1], out_bf16=True, out=out), iters, flush,
+                          stream)
     tflops = 2.0 * n ** 3 / (ms * 1e-3) / 1e12
-    del ops, out, flush
+    tflops_flush = 2.0 * n ** 3 / (ms_flush * 1e-3) / 1e12
+    del ops, out, flush, g
     torch.cuda.empty_cache()
     return {"m": n, "n": n, "k": n, "us": round(ms * 1e3, 1), "tflops": round(tflops, 1),
-            "fp4_peak_frac": round(tflops / fp4_peak, 4), "l2": "flushed before each launch"}
+            "fp4_peak_frac": round(tflops / fp4_peak, 4),
+            "l2": f"{sets} operand pairs taken in turn, more than L2 together; CUDA graph",
+            "us_l2_flushed": round(ms_flush * 1e3, 1), "fp4_peak_frac_l2_flushed": round(tflops_flush / fp4_peak, 4)}
 
 
 def preprocess_comparison(iters=3):

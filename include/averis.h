@@ -70,7 +70,8 @@ typedef enum {
   AVERIS_ERR_UNSUPPORTED_ARCH = 2,   /* current device is not sm_10x */
   AVERIS_ERR_CUDA = 3,               /* a CUDA runtime/driver call failed */
   AVERIS_ERR_WORKSPACE_TOO_SMALL = 4,
-  AVERIS_ERR_TIMEOUT = 5             /* a device-side wait gave up (see averis_last_device_error) */
+  AVERIS_ERR_TIMEOUT = 5,            /* a device-side wait gave up (see averis_last_device_error) */
+  AVERIS_ERR_OUT_OF_BOUNDS = 6       /* a debug build's bounds check skipped an access (ditto) */
 } averis_status;
 
 /* Size of the control block at the head of every workspace (zero at rest). */
@@ -317,6 +318,14 @@ const char* averis_status_string(averis_status status);
  *   1 GEMM TMA producer, 2 GEMM MMA issuer, 3 GEMM epilogue, 4 GEMM drain,
  *   5 quantize pass (an input box or tile never arrived), 6 GEMM scale feed,
  *   7 single-read quantize (a grid-wide wait for its other CTAs gave up).
+ * In a library built with its bounds checks (averis_debug_checks() == 1) the
+ * word can also hold 100 + site of the first access a check caught and
+ * skipped; it then returns AVERIS_ERR_OUT_OF_BOUNDS.  Sites: 1-3 statistics
+ * pass (partials, their combine, the mean), 4-6 mean CTAs (mean loads, NVFP4
+ * mean, dequantized mean), 7-8 rank-one row (weights, output), 9-11 quantize
+ * pass (row codes, column codes, scale atoms), 12 single-read quantize
+ * partials, 13 GEMM epilogue vectors, 14 a TMA copy's inner coordinate off the
+ * 16-byte rule, 15 averis_rank1's output.
  * The results of the calls that timed out are invalid.  When it reports a
  * timeout it also zeroes the control block of averis_quantize_noalloc's
  * scratch, whose callers cannot reach it.
@@ -339,6 +348,23 @@ averis_status averis_debug_starve_next_quantize(long long wait_cycles);
 
 /* Library version, major*10000 + minor*100 + patch. */
 int averis_version(void);
+
+/*
+ * averis_debug_checks -- whether this build checks its kernels' memory
+ * accesses.  The method has no counterpart of this call: it serves testing on
+ * machines without a memory checker.  Built with -DAVERIS_DEBUG (the
+ * libaveris_debug.so of the build script), every kernel checks each global
+ * address it computes against the extent of its buffer, and the inner
+ * coordinate of each TMA copy against the 16-byte rule; a failed check skips
+ * the access and records its site (averis_last_device_error).  Returns 0 for
+ * a release build (no checks compiled in).  In a debug build it first runs a
+ * one-thread self-test on the current device -- the bounds predicate on
+ * in-range and out-of-range (offset, extent) pairs, with no memory access,
+ * and one recorded site read back and cleared -- and returns 1 if it passed,
+ * -1 if not, or if an error was already pending (which it leaves in place)
+ * or a CUDA call failed.  Synchronizes the device.
+ */
+int averis_debug_checks(void);
 
 #ifdef __cplusplus
 }

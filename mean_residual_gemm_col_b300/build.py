@@ -1,6 +1,8 @@
-"""Build libaveris.so (sm_103a) in-tree with nvcc.
+"""Build libaveris.so (sm_103a) in-tree with nvcc, and its bounds-checked
+debug variant libaveris_debug.so (-DAVERIS_DEBUG: every global address a
+kernel computes is checked against its buffer, see csrc/debug.cuh).
 
-Usage: python -m mean_residual_gemm_col_b300.build [--force]
+Usage: python -m mean_residual_gemm_col_b300.build [--force] [--debug]
 """
 
 from __future__ import annotations
@@ -14,9 +16,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(PKG, "libaveris.so")
+DEBUG_LIB = os.path.join(PKG, "libaveris_debug.so")
 
 SOURCES = [os.path.join(CSRC, "averis_api.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "quant.cuh", "gemm.cuh")] + [
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "quant.cuh", "gemm.cuh", "debug.cuh")] + [
     os.path.join(INCLUDE, "averis.h")
 ]
 
@@ -35,26 +38,28 @@ def nvcc() -> str:
     return "nvcc"
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in DEPENDS)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile the library if any source is newer than it; return its path."""
-    if not force and up_to_date():
-        return LIB
-    tmp = LIB + ".tmp"
-    cmd = [nvcc(), *NVCC_FLAGS, "-I" + INCLUDE, "-o", tmp, *SOURCES]
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile the library (debug: the bounds-checked variant) if any source is
+    newer than it; return its path."""
+    lib = DEBUG_LIB if debug else LIB
+    if not force and up_to_date(lib):
+        return lib
+    tmp = lib + ".tmp"
+    cmd = [nvcc(), *NVCC_FLAGS, *(["-DAVERIS_DEBUG"] if debug else []), "-I" + INCLUDE, "-o", tmp, *SOURCES]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd), flush=True)
     subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

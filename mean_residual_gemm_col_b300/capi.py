@@ -25,7 +25,8 @@ AVERIS_HADAMARD16 = 2
 AVERIS_OUT_BF16 = 4
 
 STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported architecture", 3: "CUDA error",
-          4: "workspace too small", 5: "device-side wait timed out"}
+          4: "workspace too small", 5: "device-side wait timed out",
+          6: "out-of-range access caught by a debug-build check"}
 
 #: every function declared in include/averis.h
 EXPORTS = (
@@ -34,6 +35,7 @@ EXPORTS = (
     "averis_gemm", "averis_linear_fwd_workspace_bytes", "averis_linear_bwd_workspace_bytes",
     "averis_linear_fwd", "averis_linear_bwd", "nvfp4_linear_fwd", "nvfp4_linear_bwd",
     "averis_status_string", "averis_last_device_error", "averis_version", "averis_quantize_noalloc",
+    "averis_debug_checks",
     "averis_grouped_linear_fwd_workspace_bytes", "averis_grouped_linear_bwd_workspace_bytes",
     "averis_grouped_linear_fwd", "averis_grouped_linear_bwd", "averis_debug_starve_next_quantize",
 )
@@ -85,6 +87,7 @@ def _declare(lib):
         "averis_grouped_linear_fwd": (I, [P, P, I64, I64, I64, P, U, P, P, P, SZ, P]),
         "averis_grouped_linear_bwd": (I, [P, P, I64, I64, I64, P, P, U, P, P, P, SZ, P]),
         "averis_debug_starve_next_quantize": (I, [ctypes.c_longlong]),
+        "averis_debug_checks": (I, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -422,13 +425,14 @@ class GroupedLinear:
 
 
 def averis_last_device_error(device=None) -> int:
-    """0, or the code of the device-side wait that gave up (then clears it)."""
+    """0, or the code of the device-side wait that gave up, or (debug build)
+    100 + the site of a bounds check that caught an access; then clears it."""
     import torch
 
     lib = load()
     where = ctypes.c_int(0)
     st = lib.averis_last_device_error(_stream(device or torch.cuda.current_device()), ctypes.byref(where))
-    if st not in (0, 5):
+    if st not in (0, 5, 6):
         _check(st, "averis_last_device_error")
     return where.value
 

@@ -150,6 +150,44 @@ averis_status set_attrs() {
   return AVERIS_OK;
 }
 
+#ifdef AVERIS_DEBUG
+// The bounds predicate on fixed (offset, extent, bytes) cases -- addresses
+// built from a fake base, never dereferenced -- and one recorded site.
+__device__ int g_dbg_selftest[8];
+
+__global__ void debug_self_test_kernel(int* err) {
+  const char* base = reinterpret_cast<const char*>(0x10000);
+  g_dbg_selftest[0] = dbg_inside(base, base, 64, 64);       // whole buffer: in
+  g_dbg_selftest[1] = dbg_inside(base + 48, base, 64, 16);  // last 16 bytes: in
+  g_dbg_selftest[2] = dbg_inside(base + 56, base, 64, 16);  // crosses the end: out
+  g_dbg_selftest[3] = dbg_inside(base - 4, base, 64, 4);    // before the start: out
+  g_dbg_selftest[4] = dbg_inside(base + 64, base, 64, 1);   // one past the end: out
+  g_dbg_selftest[5] = dbg_inside(base, nullptr, 64, 4);     // no buffer: out
+  g_dbg_selftest[6] = dbg_in(err, base + 64, base, 64, 4, kSiteSelfTest);  // out, recorded
+  g_dbg_selftest[7] = 1;
+}
+
+// 1: predicate and recorder work; -1: they do not, an error was pending, or CUDA failed.
+int debug_self_test() {
+  DeviceInfo* dev = nullptr;
+  if (device_info(&dev) != AVERIS_OK) return -1;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess || v != 0) return -1;
+  debug_self_test_kernel<<<1, 1>>>(dev->err_word);
+  if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return -1;
+  int got[8] = {};
+  if (cudaMemcpyFromSymbol(got, g_dbg_selftest, sizeof(got)) != cudaSuccess) return -1;
+  if (cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int)) != cudaSuccess) return -1;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof(int)) != cudaSuccess) return -1;
+  const int want[8] = {1, 1, 0, 0, 0, 0, 0, 1};
+  for (int i = 0; i < 8; ++i)
+    if (got[i] != want[i]) return -1;
+  return v == kErrBoundsBase + kSiteSelfTest ? 1 : -1;
+}
+#endif
+
 // ------------------------------------------------------------ geometry --
 
 struct StatsGeom {
@@ -803,7 +841,7 @@ averis_status rank1_impl(const averis_nvfp4* mu_q, const averis_nvfp4* w, float*
   if (launch_pdl(rank1_gemv_kernel, dim3((unsigned)cdiv(N, 8)), dim3(256), 0, s, (const uint8_t*)mu_q->codes,
                  (const uint8_t*)mu_q->scales, (const float*)mu_q->tensor_scale, (const uint8_t*)w->codes,
                  (const uint8_t*)w->scales, (const float*)w->tensor_scale, averis_nvfp4_ld(K), N, K, cdiv(K, 64),
-                 out) != cudaSuccess)
+                 out, dev->err_word) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }
@@ -1185,6 +1223,7 @@ const char* averis_status_string(averis_status status) {
     case AVERIS_ERR_CUDA: return "CUDA error";
     case AVERIS_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
     case AVERIS_ERR_TIMEOUT: return "device-side wait timed out";
+    case AVERIS_ERR_OUT_OF_BOUNDS: return "out-of-range access caught by a debug-build check";
   }
   return "unknown status";
 }
@@ -1205,7 +1244,7 @@ averis_status averis_last_device_error(cudaStream_t stream, int* where) {
     if (noalloc_reset_ctrl(stream) != AVERIS_OK) return AVERIS_ERR_CUDA;
   }
   if (where != nullptr) *where = v;
-  return v == 0 ? AVERIS_OK : AVERIS_ERR_TIMEOUT;
+  return v == 0 ? AVERIS_OK : v >= kErrBoundsBase ? AVERIS_ERR_OUT_OF_BOUNDS : AVERIS_ERR_TIMEOUT;
 }
 
 averis_status averis_debug_starve_next_quantize(long long wait_cycles) {
@@ -1216,6 +1255,14 @@ averis_status averis_debug_starve_next_quantize(long long wait_cycles) {
 }
 
 int averis_version(void) { return 20000; }
+
+int averis_debug_checks(void) {
+#ifndef AVERIS_DEBUG
+  return 0;
+#else
+  return debug_self_test();
+#endif
+}
 
 }  // extern "C"
 

@@ -48,6 +48,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 
+#include "debug.cuh"
 #include "ptx.cuh"
 
 namespace averis {
@@ -294,10 +295,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
           // both CTAs' operand halves complete on the leader's stage barrier
           const uint32_t full_leader = ptx::mapa(ptx::smem_u32(&full[stage]), 0);
           if (cta == 0) ptx::mbar_arrive_expect_tx(&full[stage], 2u * (uint32_t)(Cfg::A_BYTES + Cfg::B_BYTES));
-          ptx::tma_load_2d_pair(smem + Cfg::OFF_A + stage * Cfg::A_BYTES, tmA, kt * Cfg::BKB,
-                                mt * Cfg::PM + (int)cta * Cfg::BM, full_leader);
-          ptx::tma_load_2d_pair(smem + Cfg::OFF_B + stage * Cfg::B_BYTES, tmB, kt * Cfg::BKB,
-                                nt * BN + (int)cta * Cfg::BNH, full_leader);
+          if (AVERIS_DBG_TMA_X(p.err, (int64_t)kt * Cfg::BKB, 1)) {
+            ptx::tma_load_2d_pair(smem + Cfg::OFF_A + stage * Cfg::A_BYTES, tmA, kt * Cfg::BKB,
+                                  mt * Cfg::PM + (int)cta * Cfg::BM, full_leader);
+            ptx::tma_load_2d_pair(smem + Cfg::OFF_B + stage * Cfg::B_BYTES, tmB, kt * Cfg::BKB,
+                                  nt * BN + (int)cta * Cfg::BNH, full_leader);
+          }
           issued |= 1u << stage;
           if (++stage == STAGES) {
             stage = 0;
@@ -456,15 +459,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
       const bool has_outer = gg.row_vec != nullptr;
       const int row0 = mt * Cfg::PM + (int)cta * Cfg::BM + q * 32;
       const int row = row0 + lane;
-      const float rterm = (has_outer && row < gg.M) ? gg.outer * __ldg(gg.row_vec + row) : 0.f;
+      const float rterm = (has_outer && row < gg.M &&
+                           AVERIS_DBG_IN(p.err, gg.row_vec + row, gg.row_vec, (int64_t)gg.M * 4, 4, kSiteGemmVectors))
+                              ? gg.outer * __ldg(gg.row_vec + row)
+                              : 0.f;
       // this tile's vector entries -> SMEM (one buffer: the barrier at the end of
       // the previous tile kept every warp from writing while another still read)
       float* cadd_s = vec_base;
       float* cvec_s = cadd_s + BN;
       for (int c = et; c < BN; c += 32 * EPI_WARPS) {
         const int col = nt * BN + c;
-        cadd_s[c] = (has_add && col < gg.N) ? __ldg(gg.col_add + col) : 0.f;
-        cvec_s[c] = (has_outer && col < gg.N) ? __ldg(gg.col_vec + col) : 0.f;
+        cadd_s[c] = (has_add && col < gg.N &&
+                     AVERIS_DBG_IN(p.err, gg.col_add + col, gg.col_add, (int64_t)gg.N * 4, 4, kSiteGemmVectors))
+                        ? __ldg(gg.col_add + col)
+                        : 0.f;
+        cvec_s[c] = (has_outer && col < gg.N &&
+                     AVERIS_DBG_IN(p.err, gg.col_vec + col, gg.col_vec, (int64_t)gg.N * 4, 4, kSiteGemmVectors))
+                        ? __ldg(gg.col_vec + col)
+                        : 0.f;
       }
       // one thread waits for the accumulator; the barrier hands its verdict (and
       // the staged vectors) to all epilogue warps, so they leave the loop together
@@ -490,7 +502,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          ptx::tma_store_2d(tmD, stage_buf, col0, row0);
+          if (AVERIS_DBG_TMA_X(p.err, col0, gg.bf16 ? 2 : 4)) ptx::tma_store_2d(tmD, stage_buf, col0, row0);
           ptx::bulk_commit();
         }
       };

@@ -25,6 +25,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include "debug.cuh"
 #include "ptx.cuh"
 
 namespace averis {
@@ -380,8 +381,9 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
         for (int64_t k = 0; k < kStatsBufs && k < nbox; ++k) {
           const uint32_t b = (it + (uint32_t)k) % kStatsBufs;
           ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
-          ptx::tma_load_2d_hint(ring + b * kStatsBox, &tmX, strip * 64,
-                                (int32_t)(p.row_base + rb0 + k * kStatsBoxRows), &s_full[b], keep);
+          if (AVERIS_DBG_TMA_X(p.err, (int64_t)strip * 64, 2))
+            ptx::tma_load_2d_hint(ring + b * kStatsBox, &tmX, strip * 64,
+                                  (int32_t)(p.row_base + rb0 + k * kStatsBoxRows), &s_full[b], keep);
           s_issued = (int)k + 1;
         }
     }
@@ -431,8 +433,9 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
           s_done[b] = 0;
           if (k + kStatsBufs < nbox) {
             ptx::mbar_arrive_expect_tx(&s_full[b], (uint32_t)kStatsBox);
-            ptx::tma_load_2d_hint(ring + b * kStatsBox, &tmX, strip * 64,
-                                  (int32_t)(p.row_base + rb0 + (k + kStatsBufs) * kStatsBoxRows), &s_full[b], keep);
+            if (AVERIS_DBG_TMA_X(p.err, (int64_t)strip * 64, 2))
+              ptx::tma_load_2d_hint(ring + b * kStatsBox, &tmX, strip * 64,
+                                    (int32_t)(p.row_base + rb0 + (k + kStatsBufs) * kStatsBoxRows), &s_full[b], keep);
             s_issued = (int)(k + kStatsBufs) + 1;
           }
         }
@@ -487,7 +490,8 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
         m1 = fmaxf(m1, s_mx[w][tid]);
         m2 = fminf(m2, s_mn[w][tid]);
       }
-      if (col < p.C)
+      if (col < p.C && AVERIS_DBG_IN(p.err, p.part + (int64_t)by * p.C + col, p.part, (int64_t)nby * p.C * 16, 16,
+                                     kSiteStatsPartial))
         *reinterpret_cast<float4*>(p.part + (int64_t)by * p.C + col) = make_float4(acc.hi, acc.lo, m1, m2);
     }
     __syncthreads();
@@ -518,8 +522,10 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
         float4 q[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j)
-          q[j] = rb + 4 * j < nrb ? __ldcg(reinterpret_cast<const float4*>(p.part + (int64_t)(rb + 4 * j) * p.C + col))
-                                  : make_float4(0.f, 0.f, -FLT_MAX, FLT_MAX);
+          q[j] = rb + 4 * j < nrb && AVERIS_DBG_IN(p.err, p.part + (int64_t)(rb + 4 * j) * p.C + col, p.part,
+                                                   (int64_t)nrb * p.C * 16, 16, kSiteStatsCombine)
+                     ? __ldcg(reinterpret_cast<const float4*>(p.part + (int64_t)(rb + 4 * j) * p.C + col))
+                     : make_float4(0.f, 0.f, -FLT_MAX, FLT_MAX);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           acc = df_add(acc, F2{q[j].x, q[j].y});
@@ -538,7 +544,7 @@ __device__ __forceinline__ void colstats_body(const CUtensorMap& tmX, const Stat
       const float M2 = fminf(fminf(s_mn[0][cl], s_mn[1][cl]), fminf(s_mn[2][cl], s_mn[3][cl]));
       if (p.split) {
         const float mu = df_div_count(S, Rf);
-        p.mu[col] = mu;
+        if (AVERIS_DBG_IN(p.err, p.mu + col, p.mu, p.C * 4, 4, kSiteStatsMean)) p.mu[col] = mu;
         a_res = fmaxf(a_res, fmaxf(fabsf(__fsub_rn(M1, mu)), fabsf(__fsub_rn(M2, mu))));
       } else {
         a_res = fmaxf(a_res, fmaxf(fabsf(M1), fabsf(M2)));
@@ -590,7 +596,8 @@ __device__ float quantize_mean(const P& p, bool write_global, uint8_t* s_codes, 
   for (int64_t b = threadIdx.x; b < nb; b += 256) {
     float v[16];
 #pragma unroll
-    for (int e = 0; e < 16; ++e) v[e] = __ldcg(p.mu + 16 * b + e);
+    for (int e = 0; e < 16; ++e)
+      v[e] = AVERIS_DBG_IN(p.err, p.mu + 16 * b + e, p.mu, p.C * 4, 4, kSiteMeanLoad) ? __ldcg(p.mu + 16 * b + e) : 0.f;
     if (had) fwht16(v);
 #pragma unroll
     for (int e = 0; e < 16; ++e) a = fmaxf(a, fabsf(v[e]));
@@ -601,7 +608,9 @@ __device__ float quantize_mean(const P& p, bool write_global, uint8_t* s_codes, 
     float v[16];
 #pragma unroll
     for (int e = 0; e < 16; e += 4) {
-      const float4 m4 = __ldcg(reinterpret_cast<const float4*>(p.mu + 16 * b + e));
+      const float4 m4 = AVERIS_DBG_IN(p.err, p.mu + 16 * b + e, p.mu, p.C * 4, 16, kSiteMeanLoad)
+                            ? __ldcg(reinterpret_cast<const float4*>(p.mu + 16 * b + e))
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
       v[e] = m4.x;
       v[e + 1] = m4.y;
       v[e + 2] = m4.z;
@@ -612,8 +621,10 @@ __device__ float quantize_mean(const P& p, bool write_global, uint8_t* s_codes, 
     *reinterpret_cast<uint2*>(s_codes + 8 * b) = make_uint2(q.lo, q.hi);
     s_scales[b] = (uint8_t)q.scale;
     if (!write_global) continue;
-    *reinterpret_cast<uint2*>(p.mu_codes + 8 * b) = make_uint2(q.lo, q.hi);
-    p.mu_scales[scale_offset(0, b, p.mu_kc)] = (uint8_t)q.scale;
+    if (AVERIS_DBG_IN(p.err, p.mu_codes + 8 * b, p.mu_codes, (p.C + 63) / 64 * 32, 8, kSiteMeanCodes))
+      *reinterpret_cast<uint2*>(p.mu_codes + 8 * b) = make_uint2(q.lo, q.hi);
+    if (AVERIS_DBG_IN(p.err, p.mu_scales + scale_offset(0, b, p.mu_kc), p.mu_scales, 512 * p.mu_kc, 1, kSiteMeanCodes))
+      p.mu_scales[scale_offset(0, b, p.mu_kc)] = (uint8_t)q.scale;
     const float sc = e4m3_value(q.scale);
     float d[16];
 #pragma unroll
@@ -624,7 +635,8 @@ __device__ float quantize_mean(const P& p, bool write_global, uint8_t* s_codes, 
     if (had) fwht16(d);
 #pragma unroll
     for (int e = 0; e < 16; e += 4)
-      *reinterpret_cast<float4*>(p.mu_hat + 16 * b + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
+      if (AVERIS_DBG_IN(p.err, p.mu_hat + 16 * b + e, p.mu_hat, p.C * 4, 16, kSiteMeanHat))
+        *reinterpret_cast<float4*>(p.mu_hat + 16 * b + e) = make_float4(d[e], d[e + 1], d[e + 2], d[e + 3]);
   }
   __syncthreads();
   return s_g;
@@ -685,12 +697,17 @@ __device__ void rank1_rows(const P& p, int64_t n0, int64_t n1, const uint8_t* s_
       for (int i = 0; i < RW; ++i) {
         const int64_t n = min(nr + i, n1 - 1);
         const uint8_t* wrow = p.w_codes + n * p.w_ld + 16 * j;
-        wc[i] = two ? __ldg(reinterpret_cast<const uint4*>(wrow))
-                    : make_uint4(__ldg(reinterpret_cast<const uint32_t*>(wrow)),
-                                 __ldg(reinterpret_cast<const uint32_t*>(wrow + 4)), 0u, 0u);
+        wc[i] = !AVERIS_DBG_IN(p.err, wrow, p.w_codes, p.w_rows * p.w_ld, two ? 16 : 8, kSiteRank1Weight)
+                    ? make_uint4(0u, 0u, 0u, 0u)
+                : two ? __ldg(reinterpret_cast<const uint4*>(wrow))
+                      : make_uint4(__ldg(reinterpret_cast<const uint32_t*>(wrow)),
+                                   __ldg(reinterpret_cast<const uint32_t*>(wrow + 4)), 0u, 0u);
         // blocks 2j, 2j+1 of a row sit in adjacent bytes of one scale atom
         const uint8_t* sp = p.w_scales + scale_offset(n, 2 * j, p.w_kc);
-        wsc[i] = two ? __ldg(reinterpret_cast<const uint16_t*>(sp)) : __ldg(sp);
+        wsc[i] = !AVERIS_DBG_IN(p.err, sp, p.w_scales, 512 * ((p.w_rows + 127) / 128) * p.w_kc, two ? 2 : 1,
+                                kSiteRank1Weight)
+                     ? 0u
+                 : two ? __ldg(reinterpret_cast<const uint16_t*>(sp)) : __ldg(sp);
       }
       const uint4 mc = two ? *reinterpret_cast<const uint4*>(s_codes + 16 * j)
                            : make_uint4(*reinterpret_cast<const uint32_t*>(s_codes + 16 * j),
@@ -718,7 +735,7 @@ __device__ void rank1_rows(const P& p, int64_t n0, int64_t n1, const uint8_t* s_
 #pragma unroll
       for (int i = 1; i < RW; ++i)
         if (lane == i) v = acc[i];
-      p.r_out[nr + lane] = v * s;
+      if (AVERIS_DBG_IN(p.err, p.r_out + nr + lane, p.r_out, p.w_rows * 4, 4, kSiteRank1Out)) p.r_out[nr + lane] = v * s;
     }
   }
 }
@@ -901,7 +918,9 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
       } else {
         uint32_t lo, hi;
         const uint32_t sc = quant16_tab(rx, den_row, pos_row, inv_s, lo, hi);
-        if (valid) *reinterpret_cast<uint2*>(p.row_codes + gr * p.row_ld + ch / 2 + 8 * kb) = make_uint2(lo, hi);
+        if (valid && AVERIS_DBG_IN(p.err, p.row_codes + gr * p.row_ld + ch / 2 + 8 * kb, p.row_codes, p.R * p.row_ld, 8,
+                                   kSiteRowCodes))
+          *reinterpret_cast<uint2*>(p.row_codes + gr * p.row_ld + ch / 2 + 8 * kb) = make_uint2(lo, hi);
         stage[half * 512 + 16 * (row & 31) + 4 * (row >> 5) + kb] = (uint8_t)sc;
       }
     }
@@ -963,7 +982,8 @@ __device__ __forceinline__ void quant_tile_warp(const QuantParams& p, const uint
       } else {
         uint32_t lo, hi;
         const uint32_t sc = quant16_tab(rx, den_col, pos_col, inv_s + 128, lo, hi);
-        if (cvalid && (!EDGE || off < p.col_ld))
+        if (cvalid && (!EDGE || off < p.col_ld) &&
+            AVERIS_DBG_IN(p.err, p.col_codes + (c0 + cc) * p.col_ld + off, p.col_codes, p.C * p.col_ld, 8, kSiteColCodes))
           *reinterpret_cast<uint2*>(p.col_codes + (c0 + cc) * p.col_ld + off) = make_uint2(lo, hi);
         stage[1024 + (rq >> 1) * 512 + 16 * (cc & 31) + 4 * (cc >> 5) + 2 * (rq & 1) + rb] = (uint8_t)sc;
       }
@@ -1010,6 +1030,7 @@ __device__ __forceinline__ void split_quant_body(const CUtensorMap& tmX, const Q
     const int32_t y = (int32_t)(p.row_base + (int64_t)tr * kQTile);
     // the last read of X in this call (the stats pass kept it in L2)
     const uint64_t last_use = ptx::l2_policy_evict_first();
+    if (!AVERIS_DBG_TMA_X(p.err, (int64_t)tc * kQTile, 2)) return;
     ptx::tma_load_2d_hint(sm + b * kQTileBytes, &tmX, tc * kQTile, y, &full[b], last_use);
     ptx::tma_load_2d_hint(sm + b * kQTileBytes + kQHalf, &tmX, tc * kQTile + 64, y, &full[b], last_use);
   };
@@ -1108,7 +1129,10 @@ __device__ __forceinline__ void split_quant_body(const CUtensorMap& tmX, const Q
           if (on) {
             uint8_t* dst = is_col ? p.col_scales + ((int64_t)tc * p.col_kc + kc) * 512
                                   : p.row_scales + ((int64_t)tr * p.row_kc + kc) * 512;
-            *reinterpret_cast<uint4*>(dst + 16 * lane) = *reinterpret_cast<const uint4*>(stage + 512 * a + 16 * lane);
+            if (AVERIS_DBG_IN(p.err, dst + 16 * lane, is_col ? p.col_scales : p.row_scales,
+                              is_col ? 512 * ((p.C + 127) / 128) * p.col_kc : 512 * ((p.R + 127) / 128) * p.row_kc, 16,
+                              kSiteScaleAtoms))
+              *reinterpret_cast<uint4*>(dst + 16 * lane) = *reinterpret_cast<const uint4*>(stage + 512 * a + 16 * lane);
           }
         }
         __syncwarp();
@@ -1211,7 +1235,9 @@ static_assert(kQOffMu + 4 * 128 * 16 <= kQOffBar, "tile partials do not fit the 
 // quarters are combined as hi + lo pairs in a fixed order.  Rows at or past R
 // count neither in the sum nor in the extremes.
 __device__ __forceinline__ void resident_tile_stats(const uint8_t* buf, float4* scratch, int64_t r0, int64_t c0,
-                                                    int64_t R, int64_t C, ColPartial* part_row) {
+                                                    int64_t R, int64_t C, ColPartial* part_row,
+                                                    [[maybe_unused]] const ColPartial* part,
+                                                    [[maybe_unused]] int64_t part_extent, [[maybe_unused]] int* err) {
   const int tid = threadIdx.x;
   const int cp = tid & 63, rq = tid >> 6;
   const uint8_t* hb = buf + (cp >> 5) * kQHalf;
@@ -1257,7 +1283,8 @@ __device__ __forceinline__ void resident_tile_stats(const uint8_t* buf, float4* 
       m1 = fmaxf(m1, q.z);
       m2 = fminf(m2, q.w);
     }
-    *reinterpret_cast<float4*>(part_row + c0 + tid) = make_float4(acc.hi, acc.lo, m1, m2);
+    if (AVERIS_DBG_IN(err, part_row + c0 + tid, part, part_extent, 16, kSiteResidentPart))
+      *reinterpret_cast<float4*>(part_row + c0 + tid) = make_float4(acc.hi, acc.lo, m1, m2);
   }
   __syncthreads();  // scratch is free for the next tile
 }
@@ -1277,7 +1304,10 @@ __device__ __forceinline__ float resident_combine(const QuantParams& p, const Co
     F2 acc{0.f, 0.f};
     float m1 = -FLT_MAX, m2 = FLT_MAX;
     for (int j = lane; j < tiles_r; j += 32) {
-      const float4 q = __ldcg(reinterpret_cast<const float4*>(part + (int64_t)j * p.C + c));
+      const float4 q = AVERIS_DBG_IN(p.err, part + (int64_t)j * p.C + c, part, (int64_t)tiles_r * p.C * 16, 16,
+                                     kSiteResidentPart)
+                           ? __ldcg(reinterpret_cast<const float4*>(part + (int64_t)j * p.C + c))
+                           : make_float4(0.f, 0.f, -FLT_MAX, FLT_MAX);
       acc = df_add(acc, F2{q.x, q.y});
       m1 = fmaxf(m1, q.z);
       m2 = fminf(m2, q.w);
@@ -1291,7 +1321,7 @@ __device__ __forceinline__ float resident_combine(const QuantParams& p, const Co
     }
     if (mu_out != nullptr) {
       const float mu = df_div_count(acc, Rf);
-      if (lane == 0) mu_out[c] = mu;
+      if (lane == 0 && AVERIS_DBG_IN(p.err, mu_out + c, mu_out, p.C * 4, 4, kSiteStatsMean)) mu_out[c] = mu;
       a_res = fmaxf(a_res, fmaxf(fabsf(__fsub_rn(m1, mu)), fabsf(__fsub_rn(m2, mu))));
     } else {
       a_res = fmaxf(a_res, fmaxf(fabsf(m1), fabsf(m2)));
@@ -1388,7 +1418,7 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     const int tile = tcta + landed * ntcta;
     const int tr = tile / p.tiles_c, tc = tile % p.tiles_c;
     resident_tile_stats(sm + landed * kQTileBytes, scratch, (int64_t)tr * kQTile, (int64_t)tc * kQTile, p.R, p.C,
-                        rp.part + (int64_t)tr * p.C);
+                        rp.part + (int64_t)tr * p.C, rp.part, (int64_t)p.tiles_r * p.C * 16, p.err);
   }
   if (!resident_grid_wait(p.ctrl, (unsigned)ncta, !failed, rp.grid_wait_limit, &s_ok) && !failed) {
     if (tid == 0) atomicCAS(p.err, 0, kErrQuantGrid);  // keep the cause if another CTA reported one
@@ -1462,8 +1492,11 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
       if (on) {
         uint8_t* dst = is_col ? p.col_scales + ((int64_t)tc * p.col_kc + kc) * 512
                               : p.row_scales + ((int64_t)tr * p.row_kc + kc) * 512;
-        *reinterpret_cast<uint4*>(dst + 16 * lane) =
-            *reinterpret_cast<const uint4*>(sm + kQOffStage + k * kQStageBytes + 512 * (a & 3) + 16 * lane);
+        if (AVERIS_DBG_IN(p.err, dst + 16 * lane, is_col ? p.col_scales : p.row_scales,
+                          is_col ? 512 * ((p.C + 127) / 128) * p.col_kc : 512 * ((p.R + 127) / 128) * p.row_kc, 16,
+                          kSiteScaleAtoms))
+          *reinterpret_cast<uint4*>(dst + 16 * lane) =
+              *reinterpret_cast<const uint4*>(sm + kQOffStage + k * kQStageBytes + 512 * (a & 3) + 16 * lane);
       }
     }
   }
@@ -1495,7 +1528,8 @@ __global__ void __launch_bounds__(256) rank1_gemv_kernel(const uint8_t* __restri
                                                          const uint8_t* __restrict__ w_codes,
                                                          const uint8_t* __restrict__ w_scales,
                                                          const float* __restrict__ w_ts, int64_t w_ld, int64_t N,
-                                                         int64_t K, int64_t kc, float* __restrict__ out) {
+                                                         int64_t K, int64_t kc, float* __restrict__ out,
+                                                         [[maybe_unused]] int* err) {
   __shared__ float lut[16];
   ptx::pdl_wait_and_release();
   if (threadIdx.x < 16) lut[threadIdx.x] = e2m1_val(threadIdx.x);
@@ -1519,7 +1553,7 @@ __global__ void __launch_bounds__(256) rank1_gemv_kernel(const uint8_t* __restri
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (lane == 0) out[r] = (acc * __ldg(mu_ts)) * __ldg(w_ts);
+  if (lane == 0 && AVERIS_DBG_IN(err, out + r, out, N * 4, 4, kSiteGemvOut)) out[r] = (acc * __ldg(mu_ts)) * __ldg(w_ts);
 }
 
 }  // namespace averis
