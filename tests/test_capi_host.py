@@ -34,6 +34,18 @@ def test_every_declared_symbol_is_exported(lib):
     assert sorted(capi.EXPORTS) == names
 
 
+def test_debug_build_exports_the_same_symbols():
+    """The bounds-checked variant is the same C ABI (only its kernels check more)."""
+    dbg = ctypes.CDLL(build.build(debug=True))
+    for n in _header_functions():
+        assert hasattr(dbg, n), n
+
+
+def test_release_build_reports_no_bounds_checks(lib):
+    # answered without touching a device: the checks are not compiled in
+    assert lib.averis_debug_checks() == 0
+
+
 def test_layout_helpers_agree_with_library(lib):
     for rows, cols in [(1, 16), (200, 272), (8192, 1024), (37, 4096)]:
         assert lib.averis_nvfp4_ld(cols) == layout.code_ld(cols)
@@ -89,5 +101,6 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
 
 
 def test_status_strings(lib):
-    for code in range(6):
+    for code in range(7):
         assert capi.status_string(code)
+    assert b"debug" in lib.averis_status_string(6)
