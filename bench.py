@@ -46,16 +46,16 @@ CPU_SAMPLE_TOKENS = 256
 
 # DRAM bytes (read + write) per GEMM launch, averaged over the 12 one-GEMM
 # launches that the per-kernel timing replays (NVTX range gemm_group_timed) in
-# one ncu capture, keyed by a hash of the GEMM source the capture was taken
+# one ncu capture, keyed by a hash of the GEMM sources the capture was taken
 # on; any other source reports null.
-GEMM_TRAFFIC = {"c5223afa2900bdb6": 244.57e6 / 12}
+GEMM_TRAFFIC = {"50c6fd9531fd4445": 244.70e6 / 12}
 
 
 def gemm_traffic_per_launch():
     import hashlib
 
     h = hashlib.sha256()
-    for f in ("gemm.cuh", "ptx.cuh"):
+    for f in ("gemm.cuh", "ptx.cuh", "debug.cuh"):
         with open(os.path.join(ROOT, "mean_residual_gemm_col_b300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return GEMM_TRAFFIC.get(h.hexdigest()[:16])
