@@ -620,12 +620,20 @@ def run_ours(args, rank, ws):
         del graphs, ggraphs
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
-        line["gemm_alone"] = gemm_alone(fp4_peak)
-        line["quantize_sweep"] = quantize_sweep(peaks)
-        line["preprocess_vs_hadamard"] = preprocess_comparison()
-        line["stack_28_layers"] = stack_comparison()
-        line["moe_expert_ffn"] = moe_comparison()
-        line["quant_error_qkv"] = quant_error_diagnostic(layers[0])
+        # each extra measurement reports its own failure instead of losing the line
+        for key, fn, fargs in (("gemm_alone", gemm_alone, (fp4_peak,)), ("quantize_sweep", quantize_sweep, (peaks,)),
+                               ("preprocess_vs_hadamard", preprocess_comparison, ()),
+                               ("stack_28_layers", stack_comparison, ()), ("moe_expert_ffn", moe_comparison, ()),
+                               ("quant_error_qkv", quant_error_diagnostic, (layers[0],))):
+            try:
+                line[key] = fn(*fargs)
+            except Exception as e:  # noqa: BLE001
+                line[key] = {"error": f"{type(e).__name__}: {e}"[:300]}
+                try:
+                    torch.cuda.synchronize()
+                    torch.cuda.empty_cache()
+                except Exception:  # noqa: BLE001
+                    pass
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
     return line
