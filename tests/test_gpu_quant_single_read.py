@@ -26,3 +26,14 @@ def test_quantize_parity_on_the_single_read_path(cuda_lib):
            "tests/test_gpu_quant.py", "tests/test_gpu_timeout.py", "tests/test_gpu_linear.py"]
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
+
+
+def test_single_read_path_under_the_bounds_checks(cuda_lib):
+    """The debug build's tiny-shape run (every computed address checked, see
+    test_gpu_debug_bounds.py) with the single-read launch taking every quantize
+    call that it can, so that its partials and mean stores are checked too."""
+    env = dict(os.environ, AVERIS_SINGLE_READ_QUANTIZE="1")
+    cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider",
+           "tests/test_gpu_debug_bounds.py"]
+    r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-2000:]
