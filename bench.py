@@ -846,22 +846,19 @@ def moe_comparison(steps=3, warmup=2):
     for i, (name, m, n) in enumerate(shapes):
         x = workloads.torch_activation(31 + i, rows, m, spike=workloads.QWEN3_SPIKE, device=dev)
         _, _, d = workloads.torch_linear_case(41 + i, rows, 16, n, device=dev)
-        w = [workloads.torch_linear_case(100 * i + e, 16, m, n, device=dev)[1] for e in range(cfg["experts"])]
+        # the experts' weights stacked [E, m, n], quantized in one grouped call per step
+        w = torch.stack([workloads.torch_linear_case(100 * i + e, 16, m, n, device=dev)[1]
+                         for e in range(cfg["experts"])])
         wn = [capi.NVFP4Tensor.empty(m, n, dev) for _ in w]
         wm = [capi.NVFP4Tensor.empty(n, m, dev) for _ in w]
         gl = capi.GroupedLinear(offsets, m, n, wm, wn, dev)
         y = torch.empty(rows, n, dtype=torch.bfloat16, device=dev)
         dx = torch.empty(rows, m, dtype=torch.bfloat16, device=dev)
         lin.append((m, n, x, d, w, wn, wm, gl, y, dx))
-    lib = capi.load()
 
     def step(flags):
         for m, n, x, d, w, wn, wm, gl, y, dx in lin:
-            wsb = capi.workspace(lib.averis_quantize_workspace_bytes(m, n, 0), dev, "moe_wq")
-            for we, a, b in zip(w, wn, wm):
-                sa, sb = a.struct(), b.struct()
-                capi._check(lib.averis_quantize_weight(capi._ptr(we), m, n, 0, ctypes.byref(sa), ctypes.byref(sb),
-                                                       capi._ptr(wsb), wsb.numel(), capi._stream(dev)), "wq")
+            capi.averis_quantize_weight_grouped(w, 0, w_n=wn, w_m=wm)
             gl.fwd(x, flags, out_bf16=True, y=y)
             gl.bwd(d, flags, out_bf16=True, dx=dx)
 
@@ -870,8 +867,8 @@ def moe_comparison(steps=3, warmup=2):
     res = {"experts": cfg["experts"], "top_k": cfg["top_k"], "tokens": cfg["tokens"],
            "rows_per_expert_max": int(counts.max()), "rows_per_expert_min": int(counts.min()),
            "gflop_per_step": round(flops / 1e9, 1),
-           "note": "all experts quantized in one launch chain per tensor, expert GEMMs in one persistent launch per "
-                   "product (Y; dW; dX), pair ranges balanced by K"}
+           "note": "all experts quantized in one launch chain per tensor (weights: one grouped call per linear), "
+                   "expert GEMMs in one persistent launch per product (Y; dW; dX), pair ranges balanced by K"}
     for name, flags in (("nvfp4", 0), ("averis", capi.AVERIS_MEAN_SPLIT)):
         step(flags)
         torch.cuda.synchronize()

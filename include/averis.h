@@ -173,6 +173,28 @@ averis_status averis_quantize_weight(const void* w, int64_t m, int64_t n, unsign
                                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * averis_quantize_weight_grouped -- averis_quantize_weight for the experts of
+ * a mixture-of-experts layer, all in one launch chain (one statistics launch
+ * and one quantize launch per 64 experts, plus the rotated-maximum launch
+ * under HADAMARD16): W_bar_e = Q_b(W_e), each expert with its own tensor
+ * scales, the same bits as num_experts calls of averis_quantize_weight.
+ *  w          device bf16 [num_experts, m, n] row-major: expert e's [m, n]
+ *             weight starts at element e * m * n.
+ *  w_n, w_m   host arrays of num_experts NVFP4 descriptors (device buffers),
+ *             expert e's outputs as in averis_quantize_weight; either array
+ *             may be NULL to skip that layout (not both).
+ *  workspace  averis_quantize_weight_grouped_workspace_bytes() bytes; its
+ *             first AVERIS_GROUPED_WORKSPACE_CTRL_BYTES must be zero before
+ *             first use, and every call leaves them zero.
+ * Errors: INVALID_ARG (num_experts < 1, n % 16, an output's shape or
+ * alignment), WORKSPACE_TOO_SMALL, UNSUPPORTED_ARCH, CUDA.
+ */
+size_t averis_quantize_weight_grouped_workspace_bytes(int64_t num_experts, int64_t m, int64_t n);
+averis_status averis_quantize_weight_grouped(const void* w, int64_t num_experts, int64_t m, int64_t n,
+                                             unsigned flags, const averis_nvfp4* w_n, const averis_nvfp4* w_m,
+                                             void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * averis_rank1 -- the rank-one row r = deq(mu_q) deq(w)^T ([P1-method]: the
  * mu_bar W_bar and mu_bar W_bar^T terms), binary32.
  *  mu_q  NVFP4 [1, K];  w  NVFP4 [N, K] blocked along K;  out  device [N].

@@ -35,7 +35,7 @@ EXPORTS = (
     "averis_gemm", "averis_linear_fwd_workspace_bytes", "averis_linear_bwd_workspace_bytes",
     "averis_linear_fwd", "averis_linear_bwd", "nvfp4_linear_fwd", "nvfp4_linear_bwd",
     "averis_status_string", "averis_last_device_error", "averis_version", "averis_quantize_noalloc",
-    "averis_debug_checks",
+    "averis_debug_checks", "averis_quantize_weight_grouped_workspace_bytes", "averis_quantize_weight_grouped",
     "averis_grouped_linear_fwd_workspace_bytes", "averis_grouped_linear_bwd_workspace_bytes",
     "averis_grouped_linear_fwd", "averis_grouped_linear_bwd", "averis_debug_starve_next_quantize",
 )
@@ -88,6 +88,8 @@ def _declare(lib):
         "averis_grouped_linear_bwd": (I, [P, P, I64, I64, I64, P, P, U, P, P, P, SZ, P]),
         "averis_debug_starve_next_quantize": (I, [ctypes.c_longlong]),
         "averis_debug_checks": (I, []),
+        "averis_quantize_weight_grouped_workspace_bytes": (SZ, [I64, I64, I64]),
+        "averis_quantize_weight_grouped": (I, [P, I64, I64, I64, U, NP, NP, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -283,6 +285,28 @@ def averis_quantize_weight(w, flags: int = 0):
     a, b = w_n.struct(), w_m.struct()
     _check(lib.averis_quantize_weight(_ptr(w), m, n, flags, ctypes.byref(a), ctypes.byref(b), _ptr(ws), ws.numel(),
                                       _stream(dev)), "averis_quantize_weight")
+    return w_n, w_m
+
+
+def averis_quantize_weight_grouped(w, flags: int = 0, w_n=None, w_m=None):
+    """Per expert e of the stacked W [E, m, n]: (w_n[e] [m, n] blocked along n,
+    w_m[e] [n, m] blocked along m), as averis_quantize_weight gives, from one
+    launch chain.  Preallocated output lists may be passed in (then filled)."""
+    lib = load()
+    _check_bf16(w, "w")
+    if w.dim() != 3:
+        raise AverisError("w must be [E, m, n]")
+    E, m, n = w.shape
+    dev = w.device
+    if w_n is None:
+        w_n = [NVFP4Tensor.empty(m, n, dev) for _ in range(E)]
+    if w_m is None:
+        w_m = [NVFP4Tensor.empty(n, m, dev) for _ in range(E)]
+    ws = workspace(lib.averis_quantize_weight_grouped_workspace_bytes(E, m, n), dev, "grouped_wq")
+    a = (NVFP4Struct * E)(*[t.struct() for t in w_n])
+    b = (NVFP4Struct * E)(*[t.struct() for t in w_m])
+    _check(lib.averis_quantize_weight_grouped(_ptr(w), E, m, n, flags, a, b, _ptr(ws), ws.numel(), _stream(dev)),
+           "averis_quantize_weight_grouped")
     return w_n, w_m
 
 

@@ -977,6 +977,31 @@ averis_status averis_quantize_weight(const void* w, int64_t m, int64_t n, unsign
                        workspace_bytes, stream);
 }
 
+size_t averis_quantize_weight_grouped_workspace_bytes(int64_t num_experts, int64_t m, int64_t n) {
+  if (num_experts < 1 || m < 1 || n < 1) return 0;
+  const std::vector<int64_t> rows((size_t)num_experts, m);
+  return grouped_quant_ws_bytes(rows.data(), (int)num_experts, n);
+}
+
+averis_status averis_quantize_weight_grouped(const void* w, int64_t num_experts, int64_t m, int64_t n,
+                                             unsigned flags, const averis_nvfp4* w_n, const averis_nvfp4* w_m,
+                                             void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  if (num_experts < 1 || num_experts > (int64_t)1 << 20 || m < 1 || (w_n == nullptr && w_m == nullptr))
+    return AVERIS_ERR_INVALID_ARG;
+  if (m > ((int64_t)1 << 31) / num_experts) return AVERIS_ERR_INVALID_ARG;
+  // the experts are the row groups of one [num_experts * m, n] input
+  std::vector<GroupSpec> gs((size_t)num_experts);
+  for (int64_t e = 0; e < num_experts; ++e) {
+    GroupSpec& G = gs[(size_t)e];
+    G.row0 = e * m;
+    G.rows = m;
+    G.out_row = w_n != nullptr ? &w_n[e] : nullptr;
+    G.out_col = w_m != nullptr ? &w_m[e] : nullptr;
+  }
+  return grouped_quantize_impl(w, num_experts * m, n, flags & AVERIS_HADAMARD16, gs.data(), (int)num_experts,
+                               workspace, workspace_bytes, stream);
+}
+
 averis_status averis_rank1(const averis_nvfp4* mu_q, const averis_nvfp4* w, float* out, cudaStream_t stream) {
   return rank1_impl(mu_q, w, out, stream);
 }

@@ -192,3 +192,25 @@ def test_rank1_tiny(debug_lib, N, K):
     out = capi.averis_rank1(dev(mu, 1, K), dev(w, N, K)).cpu().numpy()
     _clean()
     assert rel_fro(out, (mu.dequantize() @ w.dequantize().T)[0]) < 1e-6
+
+
+@pytest.mark.parametrize("m,n", [(16, 16), (48, 32), (32, 48)])
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_grouped_weight_quantize_tiny(debug_lib, m, n, hadamard):
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    E = 3
+    g = workloads.rng(m * 3 + n)
+    w = np.stack([workloads.weight(g, m, n) for _ in range(E)])
+    wd = to_dev_bf16(w.reshape(E * m, n)).view(E, m, n)
+    flags = capi.AVERIS_HADAMARD16 if hadamard else 0
+    g_n, g_m = capi.averis_quantize_weight_grouped(wd, flags)
+    _clean()
+    for e in range(E):
+        s_n, s_m = capi.averis_quantize_weight(wd[e].contiguous(), flags)
+        for a, b in ((g_n[e], s_n), (g_m[e], s_m)):
+            nb = -(-a.cols // 16) * 8  # the bytes that hold codes (row padding is not written)
+            assert torch.equal(a.codes[:, :nb], b.codes[:, :nb]) and torch.equal(a.scales, b.scales)
+            assert torch.equal(a.tensor_scale, b.tensor_scale)
+    _clean()

@@ -103,3 +103,63 @@ def test_grouped_moe_expert_ffn_full_shape(cuda_lib, linear):
             assert rel_fro(dx[a:b], bw.dx) < TOL, tag
             assert rel_fro(dw[e].cpu().numpy(), bw.dw) < TOL, tag
         del gl
+
+
+def _same_bits(a, b, what):
+    """Codes (the bytes that hold codes: row padding is not written), scales, tensor scale."""
+    import torch
+
+    nb = -(-a.cols // 16) * 8
+    assert torch.equal(a.codes[:, :nb], b.codes[:, :nb]), what + " codes"
+    assert torch.equal(a.scales, b.scales), what + " scales"
+    assert torch.equal(a.tensor_scale, b.tensor_scale), what + " tensor scale"
+
+
+@pytest.mark.parametrize("hadamard", [False, True])
+def test_grouped_weight_quantize_matches_per_expert(cuda_lib, hadamard):
+    """The experts' weights of a stacked [E, m, n] tensor in one launch chain:
+    every expert's two layouts and tensor scales carry the same bits as its own
+    averis_quantize_weight call, and those of one expert match the oracle."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+    from oracle import nvfp4 as onv
+    from oracle.hadamard import rotate_fp32
+
+    E, m, n = 5, 200, 144  # ragged against the 128-row tiles and 64-column strips
+    g = workloads.rng(57)
+    w = np.stack([workloads.weight(g, m, n) for _ in range(E)])
+    wd = to_dev_bf16(w.reshape(E * m, n)).view(E, m, n)
+    flags = capi.AVERIS_HADAMARD16 if hadamard else 0
+    g_n, g_m = capi.averis_quantize_weight_grouped(wd, flags)
+    torch.cuda.synchronize()
+    assert capi.averis_last_device_error() == 0
+    for e in range(E):
+        s_n, s_m = capi.averis_quantize_weight(wd[e].contiguous(), flags)
+        _same_bits(g_n[e], s_n, f"expert {e} w_n")
+        _same_bits(g_m[e], s_m, f"expert {e} w_m")
+    w2 = w[2].astype(np.float64)
+    w2t = np.zeros((n, -(-m // 16) * 16))  # the column layout's partial last block is zero-padded
+    w2t[:, :m] = w2.T
+    for dev_t, ref_in, what in ((g_n[2], w2, "w_n"), (g_m[2], w2t, "w_m")):
+        ref = onv.quantize(rotate_fp32(ref_in) if hadamard else ref_in)
+        codes, scales, s_g = dev_t.canonical()
+        assert s_g == np.float32(ref.s_g), what
+        assert np.array_equal(codes, ref.codes) and np.array_equal(scales, ref.scales), what
+
+
+def test_grouped_weight_quantize_moe_shape(cuda_lib):
+    """The benchmarked expert weights (64 experts of the gate_up linear, 2048 x 1536):
+    the grouped call gives every expert's bits of its own call."""
+    import torch
+    from mean_residual_gemm_col_b300 import capi
+
+    cfg = workloads.MOE
+    E, m, n = cfg["experts"], cfg["hidden"], 2 * cfg["ffn"]
+    wd = torch.stack([workloads.torch_linear_case(100 + e, 16, m, n, device="cuda")[1] for e in range(E)])
+    g_n, g_m = capi.averis_quantize_weight_grouped(wd)
+    for e in (0, 31, E - 1):
+        s_n, s_m = capi.averis_quantize_weight(wd[e].contiguous())
+        _same_bits(g_n[e], s_n, f"expert {e} w_n")
+        _same_bits(g_m[e], s_m, f"expert {e} w_m")
+    torch.cuda.synchronize()
+    assert capi.averis_last_device_error() == 0
