@@ -518,14 +518,15 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
   GroupedStatsParams sp{};
   GroupedQuantParams qp{};
   GroupedQuantParams ap{};  // rotated-maximum pass: tiles only
-  int n = 0, rbs = 0, ctas = 0, actas = 0;
+  int n = 0, rbs = 0, ctas = 0, mctas = 0, actas = 0;
   int64_t tiles_all = 0;
   for (int e = 0; e < ng; ++e)
     if (gs[e].rows > 0) tiles_all += cdiv(gs[e].rows, kQTile) * cdiv(C, kQTile);
   const int64_t budget = kQCtasPerSm * (int64_t)dev->sms;  // tile CTAs of one wave, shared out by tiles
-  // rank-one work of all groups: the mean CTAs of a launch take at most a
-  // quarter of a wave, shared out by the groups' weight rows (one each at
-  // least), so that mean and tile CTAs stay one resident wave
+  // rank-one work of all groups: the mean CTAs of a launch (launched ahead of
+  // every tile CTA) take at most one wave, shared out by the groups' weight
+  // rows (one each at least, about 128 K weights each at most), so that the
+  // mean phase is short and the tile CTAs start together when it ends
   int64_t w_rows_all = 0;
   for (int e = 0; e < ng; ++e)
     if (gs[e].rows > 0 && gs[e].r_w != nullptr) w_rows_all += gs[e].r_w->rows;
@@ -603,15 +604,18 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
         q.w_ld = averis_nvfp4_ld(C);
         q.w_kc = cdiv(C, 64);
         q.r_out = G.r_out;
-        q.mean_ctas =
-            (int)std::max<int64_t>(1, std::min<int64_t>(8, (budget / 4) * G.r_w->rows / std::max<int64_t>(1, w_rows_all)));
+        q.mean_ctas = (int)std::max<int64_t>(
+            1, std::min<int64_t>(std::min<int64_t>(16, cdiv(G.r_w->rows * C, (int64_t)1 << 17)),
+                                 budget * G.r_w->rows / std::max<int64_t>(1, w_rows_all)));
       }
     }
     const int64_t tiles = (int64_t)q.tiles_r * q.tiles_c;
     const int tile_ctas =
         tiles == 0 ? 0 : (int)std::max<int64_t>(1, std::min<int64_t>(tiles, budget * tiles / std::max<int64_t>(1, tiles_all)));
-    qp.cta0[n] = ctas;
-    ctas += std::max(1, q.mean_ctas + tile_ctas);
+    qp.cta0[n] = ctas;     // tile CTAs (at least one CTA per group: its last one resets its words)
+    qp.mcta0[n] = mctas;   // mean CTAs
+    ctas += q.mean_ctas + tile_ctas > 0 ? tile_ctas : 1;
+    mctas += q.mean_ctas;
     ap.g[n] = q;
     ap.g[n].mean_ctas = 0;
     ap.cta0[n] = actas;
@@ -622,6 +626,7 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
   sp.rb0[n] = rbs;
   sp.ngroups = n;
   qp.cta0[n] = ctas;
+  qp.mcta0[n] = mctas;
   qp.ngroups = n;
   ap.cta0[n] = actas;
   ap.ngroups = n;
@@ -639,7 +644,7 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
                  cudaSuccess)
     return AVERIS_ERR_CUDA;
   auto* qk = had ? split_quant_grouped_kernel<false, true> : split_quant_grouped_kernel<false, false>;
-  if (launch_pdl(qk, dim3(ctas), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess) return AVERIS_ERR_CUDA;
+  if (launch_pdl(qk, dim3(mctas + ctas), dim3(kQThreads), kQSmem, s, tx, qp) != cudaSuccess) return AVERIS_ERR_CUDA;
   return AVERIS_OK;
 }
 

@@ -1181,12 +1181,16 @@ __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
   split_quant_body<AMAX_ONLY, HAD>(tmX, p, blockIdx.x, gridDim.x);
 }
 
-// The quantize pass over the row groups of a grouped input: group e owns CTAs
-// cta0[e] .. cta0[e+1]-1 (its mean CTAs first), g[e] its rows, outputs and
-// control words.
+// The quantize pass over the row groups of a grouped input: g[e] holds group
+// e's rows, outputs and control words, and its CTAs are its mean CTAs and its
+// tile CTAs (below).
 struct GroupedQuantParams {
   QuantParams g[kMaxGroups];
+  // the launch's CTAs: first the mean CTAs of every group (group e: mcta0[e] ..
+  // mcta0[e+1]-1), then the tile CTAs (group e: mcta0[ngroups] + cta0[e] ..
+  // mcta0[ngroups] + cta0[e+1]-1); in a group the mean CTAs come first too
   int cta0[kMaxGroups + 1];
+  int mcta0[kMaxGroups + 1];
   int ngroups;
 };
 
@@ -1197,9 +1201,19 @@ static_assert(sizeof(GroupedStatsParams) + sizeof(CUtensorMap) <= 32000, "groupe
 template <bool AMAX_ONLY, bool HAD>
 __global__ void __launch_bounds__(kQThreads, kQCtasPerSm)
     split_quant_grouped_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ GroupedQuantParams gp) {
+  // all groups' mean CTAs run in the first wave and then make room for tile CTAs,
+  // which thus mostly start together instead of the last groups' starting late
+  const int nmean = gp.mcta0[gp.ngroups];
+  const int b = (int)blockIdx.x;
   int e = 0;
-  while (e + 1 < gp.ngroups && gp.cta0[e + 1] <= (int)blockIdx.x) ++e;
-  split_quant_body<AMAX_ONLY, HAD>(tmX, gp.g[e], (int)blockIdx.x - gp.cta0[e], gp.cta0[e + 1] - gp.cta0[e]);
+  if (b < nmean) {
+    while (e + 1 < gp.ngroups && gp.mcta0[e + 1] <= b) ++e;
+  } else {
+    while (e + 1 < gp.ngroups && gp.cta0[e + 1] <= b - nmean) ++e;
+  }
+  const int means = gp.mcta0[e + 1] - gp.mcta0[e];
+  const int cta = b < nmean ? b - gp.mcta0[e] : means + (b - nmean - gp.cta0[e]);
+  split_quant_body<AMAX_ONLY, HAD>(tmX, gp.g[e], cta, means + gp.cta0[e + 1] - gp.cta0[e]);
 }
 
 // ------------------------------------------------ single-read quantize ----
