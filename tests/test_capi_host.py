@@ -100,6 +100,19 @@ def test_invalid_arguments_rejected_before_any_device_work(lib):
     assert lib.averis_linear_fwd(x, 16, 16, 16, ctypes.byref(a), 0, x, ctypes.byref(st), x, 1 << 20, None) == 1
 
 
+def test_grouped_weight_quantize_host_checks(lib):
+    # sizes need no device; bad arguments are rejected before any device work
+    assert lib.averis_quantize_weight_grouped_workspace_bytes(64, 2048, 1536) > \
+        lib.averis_quantize_weight_grouped_workspace_bytes(1, 2048, 1536) > 0
+    assert lib.averis_quantize_weight_grouped_workspace_bytes(0, 16, 16) == 0
+    nv = (capi.NVFP4Struct * 2)(capi.NVFP4Struct(256, 256, 256, 16, 16), capi.NVFP4Struct(256, 256, 256, 16, 16))
+    w = ctypes.c_void_p(256)
+    assert lib.averis_quantize_weight_grouped(w, 0, 16, 16, 0, nv, None, w, 1 << 20, None) == 1  # no experts
+    assert lib.averis_quantize_weight_grouped(w, 2, 16, 16, 0, None, None, w, 1 << 20, None) == 1  # no outputs
+    assert lib.averis_quantize_weight_grouped(None, 2, 16, 16, 0, nv, None, w, 1 << 20, None) == 1  # no input
+    assert lib.averis_quantize_weight_grouped(w, 2, 16, 24, 0, nv, None, w, 1 << 20, None) == 1  # n % 16
+
+
 def test_status_strings(lib):
     for code in range(7):
         assert capi.status_string(code)
