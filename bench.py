@@ -112,7 +112,7 @@ def max_over_ranks(v, ws):
 # ----------------------------------------------------------------- clocks --
 
 class _Nvml:
-    """Read-only NVML queries through ctypes (libnvidia-ml ships with the driver)."""
+    """Read-only NVML queries through ctypes (libnvidia-ml ships with the NVIDIA driver)."""
 
     REASONS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
                "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}

@@ -372,7 +372,7 @@ averis_status averis_debug_starve_next_quantize(long long wait_cycles);
 int averis_version(void);
 
 /*
- * averis_debug_checks -- whether this build checks its kernels' memory
+ * averis_debug_checks -- whether the loaded library checks its kernels' memory
  * accesses.  The method has no counterpart of this call: it serves testing on
  * machines without a memory checker.  Built with -DAVERIS_DEBUG (the
  * libaveris_debug.so of the build script), every kernel checks each global

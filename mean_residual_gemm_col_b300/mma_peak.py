@@ -2,7 +2,7 @@
 
 Prints, per MMA form, the SM cycles one instruction takes when issued back to
 back and the rate with one CTA per SM on every SM.  The GEMM's roofline is
-reported against the measured bf16 peak times the nominal FP4:BF16
+reported against the measured bf16 peak (MEASURED_PEAKS.json) times the nominal FP4:BF16
 ratio; this measures what the NVFP4 instruction itself delivers here.
 
 Usage: python -m mean_residual_gemm_col_b300.mma_peak
