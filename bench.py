@@ -364,11 +364,12 @@ def run_step(layers, mode):
 def launches_per_step(mode):
     """Kernels one step enqueues: per linear, weight quantize (stats, quantize),
     forward (stats, quantize, GEMM), backward (stats, quantize, one GEMM launch
-    carrying both dW and dX); the Hadamard modes add the rotated-maximum pass
-    to each of the three quantizes."""
-    had = mode in ("averis_h16", "nvfp4_h16")
-    q = 3 if had else 2
-    return (q + (q + 1) + (q + 1)) * len(LINEARS)
+    carrying both dW and dX).  With the rotation, a quantize without the mean
+    split (the weights; every activation in nvfp4_h16) runs the rotated-maximum
+    pass instead of the stats pass, and one with the split runs both."""
+    w = 2
+    a = 3 if mode == "averis_h16" else 2
+    return (w + (a + 1) + (a + 1)) * len(LINEARS)
 
 
 def kernel_groups(layers):

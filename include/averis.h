@@ -145,7 +145,9 @@ size_t averis_quantize_workspace_bytes(int64_t rows, int64_t cols, unsigned flag
  *  out_col   NVFP4 [cols, rows] of T_R^T blocked along rows (output, NULL to skip).
  *  workspace device scratch of averis_quantize_workspace_bytes() bytes.
  * Kernels: a column-statistics pass, then the quantize pass (plus a rotated-
- * maximum pass under HADAMARD16).  With the environment variable
+ * maximum pass under HADAMARD16, which replaces the statistics pass when the
+ * mean split is off: both layouts then take their scales from the rotated
+ * maxima alone).  With the environment variable
  * AVERIS_SINGLE_READ_QUANTIZE=1 set when the library first sees the device,
  * an input of at most 1024 tiles of 128 x 128 whose tiles all fit the
  * resident CTAs' shared memory (two CTAs of three tiles per SM), without

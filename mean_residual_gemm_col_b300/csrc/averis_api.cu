@@ -440,7 +440,11 @@ averis_status quantize_impl(const void* x, int64_t R, int64_t C, unsigned flags,
       return AVERIS_ERR_CUDA;
     return AVERIS_OK;
   }
-  if (launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
+  // with the rotation and no mean split the column statistics would give only
+  // the unrotated maximum, which no layout uses (both take the rotated maxima):
+  // the pass runs only when it is needed (or asked to starve)
+  if ((split || !had || sp.starve) &&
+      launch_pdl(colstats_kernel, dim3(g.gx, g.nrb), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   if (had) {
     QuantParams ap = qp;  // rotated-maximum pass: tiles only
@@ -638,7 +642,9 @@ averis_status grouped_quantize_chunk(const void* x, int64_t L, int64_t C, unsign
   if (!encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, const_cast<void*>(x), (uint64_t)C, (uint64_t)L,
                  (uint64_t)C * 2, 64u, (uint32_t)kQTile))
     return AVERIS_ERR_CUDA;
-  if (launch_pdl(colstats_grouped_kernel, dim3(geo.gx, rbs), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
+  // the statistics are unused with the rotation and no mean split (see quantize_impl)
+  if ((split || !had || starve > 0) &&
+      launch_pdl(colstats_grouped_kernel, dim3(geo.gx, rbs), dim3(256), kStatsSmem, s, tstats, sp) != cudaSuccess)
     return AVERIS_ERR_CUDA;
   if (had && launch_pdl(split_quant_grouped_kernel<true, true>, dim3(actas), dim3(kQThreads), kQSmem, s, tx, ap) !=
                  cudaSuccess)
